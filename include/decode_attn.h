@@ -1,0 +1,205 @@
+/*
+ * decode_attn.h -- C ABI of libdecode_attn.so: split-KV decode attention
+ * (Flash-Decoding) for GB300 / sm_103a.
+ *
+ * The operation.  For every request b < batch, new token t < q_len and query
+ * head h < num_q_heads, with key/value head kvh = h / G and G = Hq / Hkv
+ * (contiguous GQA groups: "Capstone FlashAttention", §4.2; the inference-engine
+ * chapter "12. attention kernels", decode section):
+ *
+ *     s_j   = scale * q[b,t,h,:] . K[b, j, kvh, :]
+ *     out   = sum_j softmax(s)_j * V[b, j, kvh, :]          (bf16)
+ *     lse   = ln sum_j exp(s_j)                              (fp32)
+ *
+ * exact attention softmax(QK^T/sqrt(d))V ("Capstone FlashAttention", §1.1),
+ * over the keys j < L = seq_lens[b]; with `causal`, token t (at position
+ * L - q_len + t) only sees keys j <= L - q_len + t.  A row with no visible key
+ * gives out = 0 and lse = -inf.
+ *
+ * How.  The KV sequence of each (request, kv head) is cut into chunks of
+ * `chunk_len` tokens that run on different SMs; each chunk keeps a running
+ * max / running sum (online softmax, "Capstone FlashAttention", §1.2) and
+ * writes an fp32 partial output plus its log-sum-exp; a combine kernel merges
+ * the partials exactly ("Capstone FlashAttention", §2.3 FlashDecoding; the
+ * per-tile LSE buffer of the CUTLASS split-KV post, §4.2).  Requests whose
+ * keys fit one chunk skip the partials and the combine.
+ *
+ * Cache layouts.  K and V share one layout; head_dim is contiguous.
+ *   paged (block_table != NULL): element (page, slot, head, d) of a cache is at
+ *       page*kv_stride_page + slot*kv_stride_token + head*kv_stride_head + d;
+ *       logical token j of request b is page block_table[b*block_table_stride
+ *       + j/page_size], slot j%page_size (PagedAttention, "Capstone
+ *       FlashAttention", §4.1).
+ *   contiguous (block_table == NULL): token j of request b is at
+ *       b*kv_stride_page + j*kv_stride_token + head*kv_stride_head + d, for
+ *       j < max_seq_len.
+ * Strides are in elements; K and V base pointers must be 16-byte aligned and
+ * every KV stride a multiple of 8 elements (16 bytes).
+ *
+ * Ownership and errors.  The caller owns every buffer (device memory unless
+ * stated otherwise), including the workspace.  The library allocates nothing
+ * on the device, never synchronises the stream and may be captured in a CUDA
+ * graph.  Every function returns DA_OK (0) or a negative DA_ERR_* code; an
+ * argument error is detected on the host before anything is launched.  Data
+ * errors found on the device (a block-table entry outside [0, num_pages), a
+ * seq_len outside [0, max_seq_len], a causal request shorter than q_len) are
+ * OR-ed as DA_STATUS_* bits into *status when status != NULL; the caller reads
+ * it after synchronising.  Faulty entries never fault the GPU: a bad page id
+ * reads page 0 instead, an out-of-range length is clamped.
+ *
+ * Threading: all functions are thread-safe; calls on different streams may
+ * overlap.
+ */
+#ifndef DECODE_ATTN_H_
+#define DECODE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DECODE_ATTN_HEAD_DIM 128   /* the only supported head_dim */
+#define DECODE_ATTN_MAX_ROWS 16    /* (Hq / Hkv) * q_len must not exceed this */
+#define DECODE_ATTN_TOKEN_TILE 16  /* chunk_len and page_size are multiples */
+
+/* return codes */
+#define DA_OK 0
+#define DA_ERR_NULL_POINTER -1     /* a required pointer is NULL */
+#define DA_ERR_BAD_SHAPE -2        /* negative/zero sizes, Hq % Hkv != 0, ... */
+#define DA_ERR_HEAD_DIM -3         /* head_dim != 128 */
+#define DA_ERR_PAGE_SIZE -4        /* page_size not a positive multiple of 16 */
+#define DA_ERR_ROWS -5             /* (Hq/Hkv)*q_len > DECODE_ATTN_MAX_ROWS */
+#define DA_ERR_ALIGNMENT -6        /* pointer or stride misaligned */
+#define DA_ERR_WORKSPACE -7        /* workspace NULL or smaller than required */
+#define DA_ERR_CUDA -8             /* a CUDA runtime call or launch failed */
+#define DA_ERR_NO_DEVICE -9        /* no usable sm_103 device is current */
+#define DA_ERR_SPLITS -10          /* num_splits out of range */
+
+/* device status bits (OR-ed into *status) */
+#define DA_STATUS_BAD_PAGE 1u      /* block-table entry outside [0, num_pages) */
+#define DA_STATUS_SEQ_LEN 2u       /* seq_len < 0 or > max_seq_len (clamped) */
+#define DA_STATUS_SHORT_CAUSAL 4u  /* causal and 0 < seq_len < q_len */
+#define DA_STATUS_TIMEOUT 8u       /* an internal pipeline wait gave up */
+
+typedef struct decode_attn_params {
+  int32_t batch;              /* B >= 0 requests */
+  int32_t q_len;              /* new tokens per request, >= 1 */
+  int32_t num_q_heads;        /* Hq */
+  int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0 */
+  int32_t head_dim;           /* must be DECODE_ATTN_HEAD_DIM */
+  int32_t page_size;          /* paged: tokens per page (multiple of 16);
+                                 contiguous: ignored */
+  int32_t max_pages_per_seq;  /* paged: usable columns of block_table */
+  int32_t num_pages;          /* paged: physical pages in each cache (>= 1) */
+  int32_t max_seq_len;        /* upper bound of seq_lens in this call; the
+                                 contiguous cache holds this many tokens per
+                                 request; paged: <= max_pages_per_seq*page_size */
+  int32_t causal;             /* nonzero: causal mask among the q_len tokens */
+  float scale;                /* softmax scale, e.g. 1/sqrt(head_dim) */
+  int32_t reserved0;          /* must be 0 */
+  int64_t q_stride_batch;     /* q [B, q_len, Hq, D] element strides; */
+  int64_t q_stride_token;     /*   D contiguous, strides multiples of 8 */
+  int64_t q_stride_head;
+  int64_t o_stride_batch;     /* out [B, q_len, Hq, D] element strides */
+  int64_t o_stride_token;
+  int64_t o_stride_head;
+  int64_t kv_stride_page;     /* see "Cache layouts" above */
+  int64_t kv_stride_token;
+  int64_t kv_stride_head;
+  int64_t block_table_stride; /* elements between rows of block_table */
+} decode_attn_params;
+
+/*
+ * Fill *p with the strides of densely packed tensors:
+ *   q, out [B, q_len, Hq, D]; paged caches [num_pages, page_size, Hkv, D];
+ *   contiguous caches [B, max_seq_len, Hkv, D]; block_table [B, max_pages].
+ * scale = 1/sqrt(head_dim).  Pass page_size = 0 for a contiguous cache.
+ */
+void decode_attn_params_init(decode_attn_params *p, int32_t batch, int32_t q_len,
+                             int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t page_size,
+                             int32_t max_pages_per_seq, int32_t num_pages,
+                             int32_t max_seq_len, int32_t causal);
+
+/*
+ * Split planner (host only; reads the current device's SM count once).
+ * Picks the number of KV chunks per (request, kv head) and their length from
+ * batch x kv heads x sequence length against the SM count, so that the split
+ * kernel fills the GPU ("Capstone FlashAttention", §2.3: too few heads leave
+ * SMs idle; chunks of a few hundred tokens or more).
+ *   host_seq_lens  optional host copy of seq_lens (NULL: plan for max_seq_len)
+ *   *num_splits    out: chunks per request at max_seq_len (>= 1)
+ *   *chunk_len     out: tokens per chunk (multiple of 16)
+ */
+int decode_attn_plan(const decode_attn_params *p, const int32_t *host_seq_lens,
+                     int32_t *num_splits, int32_t *chunk_len);
+
+/*
+ * Chunk length used for a given num_splits: the smallest multiple of 16 that
+ * covers max_seq_len in num_splits chunks.  Request b uses
+ * ceil(seq_lens[b] / chunk_len) chunks (at least 1).
+ */
+int decode_attn_chunk_len(const decode_attn_params *p, int32_t num_splits,
+                          int32_t *chunk_len);
+
+/*
+ * Workspace bytes decode_attn() needs for num_splits (0 when num_splits == 1).
+ * Layout (fp32): partial outputs [B, q_len, Hq, num_splits, D], followed by
+ * partial log-sum-exps [B, q_len, Hq, num_splits] (natural log).  Partial s of
+ * a row is normalised (sum of weights 1) over its chunk's keys; an empty
+ * chunk has lse -inf.  Entries of requests that use a single chunk are not
+ * written.
+ */
+int decode_attn_workspace_bytes(const decode_attn_params *p, int32_t num_splits,
+                                size_t *bytes);
+
+/*
+ * Decode attention (the whole path: split kernel, then combine when a request
+ * spans more than one chunk).
+ *   q            bf16 [B, q_len, Hq, 128] (strides in *p)
+ *   k_cache      bf16 cache, layout per *p (16-byte aligned)
+ *   v_cache      bf16 cache, same layout as k_cache
+ *   block_table  int32 [B, block_table_stride] or NULL (contiguous cache)
+ *   seq_lens     int32 [B]: keys per request, including the q_len new tokens
+ *   out          bf16 [B, q_len, Hq, 128] (strides in *p)
+ *   lse          fp32 [B, q_len, Hq], contiguous
+ *   num_splits   chunks per request at max_seq_len; <= 0 asks the planner
+ *   workspace    device buffer of >= decode_attn_workspace_bytes() bytes
+ *                (may be NULL when that is 0)
+ *   status       optional int32 device word; DA_STATUS_* bits are OR-ed in
+ *   stream       cudaStream_t to launch on (NULL: legacy default stream)
+ * Device pointers only.  Asynchronous with respect to the host.
+ */
+int decode_attn(const decode_attn_params *p, const void *q, const void *k_cache,
+                const void *v_cache, const int32_t *block_table,
+                const int32_t *seq_lens, void *out, float *lse,
+                int32_t num_splits, void *workspace, size_t workspace_bytes,
+                int32_t *status, void *stream);
+
+/*
+ * The combine step alone: merges the partials that a split pass left in
+ * `workspace` (layout above) into out/lse, for every row whose request uses
+ * two or more chunks of `chunk_len` tokens.  M = max_s lse_s,
+ * w_s = exp(lse_s - M), out = sum_s w_s O_s / sum_s w_s, lse = M + ln sum w_s
+ * (the two-block merge of "Capstone FlashAttention", §1.2, applied to all
+ * chunks).  decode_attn() calls it itself; it is exported so that the merge
+ * can be run and checked on its own.
+ */
+int decode_attn_combine(const decode_attn_params *p, const int32_t *seq_lens,
+                        int32_t num_splits, int32_t chunk_len,
+                        const void *workspace, size_t workspace_bytes, void *out,
+                        float *lse, void *stream);
+
+/* Static description of a return code. */
+const char *decode_attn_status_string(int code);
+
+/* Number of kernel launches decode_attn() makes for these arguments (1 or 2). */
+int decode_attn_launch_count(const decode_attn_params *p, int32_t num_splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_ATTN_H_ */

@@ -1,0 +1,230 @@
+"""Thin ctypes binding of libdecode_attn.so (C ABI in include/decode_attn.h).
+
+Argument marshalling only: torch tensors supply device memory and streams,
+every step of the computation runs in the library's CUDA kernels.  The names
+mirror the C entry points.  There is no fallback: if the library is missing or
+no GPU is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libdecode_attn.so")
+
+HEAD_DIM = 128
+MAX_ROWS = 16
+TOKEN_TILE = 16
+
+DA_OK = 0
+DA_STATUS_BAD_PAGE = 1
+DA_STATUS_SEQ_LEN = 2
+DA_STATUS_SHORT_CAUSAL = 4
+DA_STATUS_TIMEOUT = 8
+
+EXPORTED_SYMBOLS = (
+    "decode_attn_params_init", "decode_attn_plan", "decode_attn_chunk_len",
+    "decode_attn_workspace_bytes", "decode_attn", "decode_attn_combine",
+    "decode_attn_status_string", "decode_attn_launch_count",
+)
+
+
+class DecodeAttnParams(ctypes.Structure):
+    """Mirror of `decode_attn_params` (same field order and types)."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("q_len", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32), ("causal", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("reserved0", ctypes.c_int32),
+        ("q_stride_batch", ctypes.c_int64), ("q_stride_token", ctypes.c_int64),
+        ("q_stride_head", ctypes.c_int64), ("o_stride_batch", ctypes.c_int64),
+        ("o_stride_token", ctypes.c_int64), ("o_stride_head", ctypes.c_int64),
+        ("kv_stride_page", ctypes.c_int64), ("kv_stride_token", ctypes.c_int64),
+        ("kv_stride_head", ctypes.c_int64), ("block_table_stride", ctypes.c_int64),
+    ]
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where} failed: {decode_attn_status_string(code)} (code {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(DecodeAttnParams)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        pi32 = ctypes.POINTER(ctypes.c_int32)
+        L.decode_attn_params_init.argtypes = [P] + [i32] * 10
+        L.decode_attn_params_init.restype = None
+        L.decode_attn_plan.argtypes = [P, vp, pi32, pi32]
+        L.decode_attn_chunk_len.argtypes = [P, i32, pi32]
+        L.decode_attn_workspace_bytes.argtypes = [P, i32, ctypes.POINTER(sz)]
+        L.decode_attn.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp, vp]
+        L.decode_attn_combine.argtypes = [P, vp, i32, i32, vp, sz, vp, vp, vp]
+        L.decode_attn_status_string.argtypes = [ctypes.c_int]
+        L.decode_attn_status_string.restype = ctypes.c_char_p
+        L.decode_attn_launch_count.argtypes = [P, i32]
+        for f in ("decode_attn_plan", "decode_attn_chunk_len", "decode_attn_workspace_bytes",
+                  "decode_attn", "decode_attn_combine", "decode_attn_launch_count"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def decode_attn_status_string(code: int) -> str:
+    return lib().decode_attn_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != DA_OK:
+        raise DecodeAttnError(code, where)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def decode_attn_params_init(batch: int, q_len: int, num_q_heads: int, num_kv_heads: int,
+                            head_dim: int = HEAD_DIM, page_size: int = 0,
+                            max_pages_per_seq: int = 0, num_pages: int = 0,
+                            max_seq_len: int = 0, causal: bool = False) -> DecodeAttnParams:
+    p = DecodeAttnParams()
+    lib().decode_attn_params_init(ctypes.byref(p), batch, q_len, num_q_heads, num_kv_heads,
+                                  head_dim, page_size, max_pages_per_seq, num_pages,
+                                  max_seq_len, 1 if causal else 0)
+    return p
+
+
+def params_from_tensors(q, k_cache, block_table=None, *, max_seq_len: int,
+                        causal: bool = False, scale: Optional[float] = None,
+                        out=None) -> DecodeAttnParams:
+    """Describe torch tensors: q/out [B, q_len, Hq, D]; k_cache paged
+    [P, page_size, Hkv, D] (block_table [B, max_pages] given) or contiguous
+    [B, S, Hkv, D].  Strides are taken from the tensors."""
+    B, T, Hq, D = q.shape
+    n0, n1, Hkv, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("head_dim of q and k_cache differ")
+    p = DecodeAttnParams()
+    p.batch, p.q_len, p.num_q_heads, p.num_kv_heads, p.head_dim = B, T, Hq, Hkv, D
+    p.max_seq_len = int(max_seq_len)
+    p.causal = 1 if causal else 0
+    p.scale = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    p.q_stride_batch, p.q_stride_token, p.q_stride_head = (int(s) for s in q.stride()[:3])
+    o = out if out is not None else q
+    p.o_stride_batch, p.o_stride_token, p.o_stride_head = (int(s) for s in o.stride()[:3])
+    p.kv_stride_page, p.kv_stride_token, p.kv_stride_head = (int(s) for s in k_cache.stride()[:3])
+    if block_table is not None:
+        p.page_size = n1
+        p.num_pages = n0
+        p.max_pages_per_seq = block_table.shape[1]
+        p.block_table_stride = int(block_table.stride(0))
+    return p
+
+
+def decode_attn_plan(p: DecodeAttnParams, host_seq_lens=None) -> Tuple[int, int]:
+    import numpy as np
+    ns, cl = ctypes.c_int32(), ctypes.c_int32()
+    arr = None
+    if host_seq_lens is not None:
+        arr = np.ascontiguousarray(host_seq_lens, dtype=np.int32)
+    _check(lib().decode_attn_plan(ctypes.byref(p),
+                                  None if arr is None else arr.ctypes.data,
+                                  ctypes.byref(ns), ctypes.byref(cl)), "decode_attn_plan")
+    return ns.value, cl.value
+
+
+def decode_attn_chunk_len(p: DecodeAttnParams, num_splits: int) -> int:
+    c = ctypes.c_int32()
+    _check(lib().decode_attn_chunk_len(ctypes.byref(p), int(num_splits), ctypes.byref(c)),
+           "decode_attn_chunk_len")
+    return c.value
+
+
+def decode_attn_workspace_bytes(p: DecodeAttnParams, num_splits: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().decode_attn_workspace_bytes(ctypes.byref(p), int(num_splits), ctypes.byref(n)),
+           "decode_attn_workspace_bytes")
+    return n.value
+
+
+def decode_attn_launch_count(p: DecodeAttnParams, num_splits: int) -> int:
+    n = lib().decode_attn_launch_count(ctypes.byref(p), int(num_splits))
+    if n < 0:
+        raise DecodeAttnError(n, "decode_attn_launch_count")
+    return n
+
+
+def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
+                causal: bool = False, scale: Optional[float] = None, num_splits: int = 0,
+                out=None, lse=None, workspace=None, status=None, stream=None,
+                params: Optional[DecodeAttnParams] = None):
+    """Run decode attention; returns (out bf16 [B, q_len, Hq, D], lse fp32
+    [B, q_len, Hq]).  Output, LSE and workspace tensors are allocated with
+    torch when not given; `num_splits <= 0` lets the library's planner choose."""
+    import torch
+
+    B, T, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
+    p = params if params is not None else params_from_tensors(
+        q, k_cache, block_table, max_seq_len=max_seq_len, causal=causal, scale=scale, out=out)
+    if num_splits <= 0:
+        num_splits, _ = decode_attn_plan(p)
+    need = decode_attn_workspace_bytes(p, num_splits)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty((need + 15) // 16 * 4, dtype=torch.float32, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().decode_attn(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                             _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse),
+                             int(num_splits), _ptr(workspace) if need > 0 else None, ws_bytes,
+                             _ptr(status), _stream_handle(stream)), "decode_attn")
+    return out, lse
+
+
+def decode_attn_combine(p: DecodeAttnParams, seq_lens, num_splits: int, chunk_len: int,
+                        workspace, out, lse, stream=None):
+    """Merge the partials held in `workspace` into out/lse (rows of requests
+    spanning two or more chunks)."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().decode_attn_combine(ctypes.byref(p), _ptr(seq_lens), int(num_splits),
+                                     int(chunk_len), _ptr(workspace), ws_bytes, _ptr(out),
+                                     _ptr(lse), _stream_handle(stream)), "decode_attn_combine")
+    return out, lse
+
+
+def workspace_views(workspace, p: DecodeAttnParams, num_splits: int):
+    """(part_o [B, q_len, Hq, S, D], part_lse [B, q_len, Hq, S]) views of a
+    workspace tensor, per the layout documented for decode_attn_workspace_bytes."""
+    S = num_splits
+    rows = p.batch * p.q_len * p.num_q_heads
+    f = workspace.view(-1)[: rows * S * (HEAD_DIM + 1)]
+    po = f[: rows * S * HEAD_DIM].view(p.batch, p.q_len, p.num_q_heads, S, HEAD_DIM)
+    pl = f[rows * S * HEAD_DIM:].view(p.batch, p.q_len, p.num_q_heads, S)
+    return po, pl

@@ -1,0 +1,413 @@
+// api.cu -- the C ABI of libdecode_attn.so (declared in include/decode_attn.h):
+// argument validation, the split planner, TMA tensor-map construction and the
+// launches of the split and combine kernels.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "decode_attn.h"
+#include "kernels.cuh"
+
+namespace {
+
+using dattn::kHeadDim;
+using dattn::kTileTokens;
+
+constexpr int kMaxDevices = 64;
+// Planner: a chunk is never shorter than this many tokens (partials and the
+// combine cost ~1.5 KB per row per chunk; a 16 KB+ chunk read keeps that small).
+constexpr int kMinChunkTokens = 256;
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int major = 0;
+  int minor = 0;
+  bool valid = false;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device_info(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DA_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.valid) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return DA_ERR_NO_DEVICE;
+    d.valid = true;
+  }
+  *out = d;
+  return DA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int rows_of(const decode_attn_params* p) {
+  return (p->num_q_heads / p->num_kv_heads) * p->q_len;
+}
+
+// Shape checks shared by every entry point.
+int check_shape(const decode_attn_params* p) {
+  if (p == nullptr) return DA_ERR_NULL_POINTER;
+  if (p->batch < 0 || p->batch > 65535 || p->q_len < 1 || p->num_q_heads < 1 ||
+      p->num_kv_heads < 1 || p->num_kv_heads > 65535 || p->max_seq_len < 0 ||
+      p->num_q_heads % p->num_kv_heads != 0 || p->reserved0 != 0 || !std::isfinite(p->scale))
+    return DA_ERR_BAD_SHAPE;
+  if (p->head_dim != DECODE_ATTN_HEAD_DIM) return DA_ERR_HEAD_DIM;
+  if (static_cast<int64_t>(p->num_q_heads / p->num_kv_heads) * p->q_len > DECODE_ATTN_MAX_ROWS)
+    return DA_ERR_ROWS;
+  return DA_OK;
+}
+
+int check_paged(const decode_attn_params* p, bool paged) {
+  if (!paged) return DA_OK;
+  if (p->page_size <= 0 || p->page_size % kTileTokens != 0) return DA_ERR_PAGE_SIZE;
+  if (p->max_pages_per_seq < 1 || p->num_pages < 1 ||
+      p->block_table_stride < p->max_pages_per_seq ||
+      static_cast<int64_t>(p->max_seq_len) >
+          static_cast<int64_t>(p->max_pages_per_seq) * p->page_size)
+    return DA_ERR_BAD_SHAPE;
+  return DA_OK;
+}
+
+int chunk_for_splits(const decode_attn_params* p, int32_t num_splits, int32_t* chunk,
+                     int32_t* splits_eff) {
+  if (num_splits < 1) return DA_ERR_SPLITS;
+  const int64_t L = p->max_seq_len;
+  int64_t c = ceil_div64(std::max<int64_t>(L, 1), num_splits);
+  c = ceil_div64(c, kTileTokens) * kTileTokens;
+  if (c > (1LL << 30)) return DA_ERR_SPLITS;
+  *chunk = static_cast<int32_t>(c);
+  *splits_eff = static_cast<int32_t>(std::max<int64_t>(1, ceil_div64(L, c)));
+  return DA_OK;
+}
+
+int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t* num_splits,
+              int32_t* chunk_len) {
+  DeviceInfo di;
+  int rc = current_device_info(&di);
+  if (rc != DA_OK) return rc;
+  const int64_t max_tiles = ceil_div64(std::max(p->max_seq_len, 1), kTileTokens);
+  const int64_t pairs = static_cast<int64_t>(std::max(p->batch, 1)) * p->num_kv_heads;
+  const int64_t slots = static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows_of(p));
+  int64_t splits = 1;
+  if (host_seq_lens == nullptr) {
+    // uniform lengths: one wave of equal chunks -- as many chunks per
+    // (request, kv head) as fit the resident CTA slots
+    if (pairs < slots) splits = slots / pairs;
+  } else {
+    // ragged lengths: aim at ~2 waves of chunks over the actual work so the
+    // long requests are cut into pieces comparable to the short ones
+    int64_t work_tiles = 0;
+    for (int32_t b = 0; b < p->batch; ++b) {
+      const int64_t Lb = std::min<int64_t>(std::max(host_seq_lens[b], 0), p->max_seq_len);
+      work_tiles += ceil_div64(Lb, kTileTokens);
+    }
+    work_tiles *= p->num_kv_heads;
+    const int64_t target_tiles = std::max<int64_t>(1, ceil_div64(work_tiles, 2 * slots));
+    splits = ceil_div64(max_tiles, target_tiles);
+  }
+  splits = std::min<int64_t>(splits, std::max<int64_t>(1, p->max_seq_len / kMinChunkTokens));
+  splits = std::max<int64_t>(1, std::min<int64_t>(splits, max_tiles));
+  int32_t chunk = 0, eff = 0;
+  rc = chunk_for_splits(p, static_cast<int32_t>(splits), &chunk, &eff);
+  if (rc != DA_OK) return rc;
+  *num_splits = eff;
+  *chunk_len = chunk;
+  return DA_OK;
+}
+
+int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p, bool paged) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return DA_ERR_CUDA;
+  // dims, innermost first: d (128), kv head, token-in-group, group
+  //   paged: group = physical page, token-in-group = slot in page
+  //   contiguous: group = request, token-in-group = token position
+  const cuuint64_t dims[4] = {
+      static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(p->num_kv_heads),
+      static_cast<cuuint64_t>(paged ? p->page_size : std::max(p->max_seq_len, 1)),
+      static_cast<cuuint64_t>(paged ? p->num_pages : std::max(p->batch, 1))};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p->kv_stride_head) * 2,
+                                 static_cast<cuuint64_t>(p->kv_stride_token) * 2,
+                                 static_cast<cuuint64_t>(p->kv_stride_page) * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTileTokens), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_ALIGNMENT;
+}
+
+bool stride_ok(int64_t s) { return s > 0 && s % 8 == 0 && s * 2 < (1LL << 40); }
+
+}  // namespace
+
+extern "C" {
+
+void decode_attn_params_init(decode_attn_params* p, int32_t batch, int32_t q_len,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t page_size, int32_t max_pages_per_seq, int32_t num_pages,
+                             int32_t max_seq_len, int32_t causal) {
+  if (p == nullptr) return;
+  std::memset(p, 0, sizeof(*p));
+  p->batch = batch;
+  p->q_len = q_len;
+  p->num_q_heads = num_q_heads;
+  p->num_kv_heads = num_kv_heads;
+  p->head_dim = head_dim;
+  p->page_size = page_size;
+  p->max_pages_per_seq = max_pages_per_seq;
+  p->num_pages = num_pages;
+  p->max_seq_len = max_seq_len;
+  p->causal = causal;
+  p->scale = head_dim > 0 ? 1.0f / std::sqrt(static_cast<float>(head_dim)) : 0.f;
+  p->q_stride_head = head_dim;
+  p->q_stride_token = static_cast<int64_t>(num_q_heads) * head_dim;
+  p->q_stride_batch = p->q_stride_token * q_len;
+  p->o_stride_head = p->q_stride_head;
+  p->o_stride_token = p->q_stride_token;
+  p->o_stride_batch = p->q_stride_batch;
+  p->kv_stride_head = head_dim;
+  p->kv_stride_token = static_cast<int64_t>(num_kv_heads) * head_dim;
+  p->kv_stride_page = p->kv_stride_token * (page_size > 0 ? page_size : max_seq_len);
+  p->block_table_stride = max_pages_per_seq;
+}
+
+int decode_attn_plan(const decode_attn_params* p, const int32_t* host_seq_lens,
+                     int32_t* num_splits, int32_t* chunk_len) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (num_splits == nullptr || chunk_len == nullptr) return DA_ERR_NULL_POINTER;
+  return plan_impl(p, host_seq_lens, num_splits, chunk_len);
+}
+
+int decode_attn_chunk_len(const decode_attn_params* p, int32_t num_splits, int32_t* chunk_len) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (chunk_len == nullptr) return DA_ERR_NULL_POINTER;
+  int32_t eff = 0;
+  return chunk_for_splits(p, num_splits, chunk_len, &eff);
+}
+
+int decode_attn_workspace_bytes(const decode_attn_params* p, int32_t num_splits, size_t* bytes) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (bytes == nullptr) return DA_ERR_NULL_POINTER;
+  int32_t chunk = 0, eff = 0;
+  rc = chunk_for_splits(p, num_splits, &chunk, &eff);
+  if (rc != DA_OK) return rc;
+  if (eff <= 1) {
+    *bytes = 0;
+    return DA_OK;
+  }
+  const size_t rows = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
+  *bytes = rows * static_cast<size_t>(eff) * (kHeadDim + 1) * sizeof(float);
+  return DA_OK;
+}
+
+int decode_attn_launch_count(const decode_attn_params* p, int32_t num_splits) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (p->batch == 0) return 0;
+  int32_t chunk = 0, eff = 0;
+  if (num_splits <= 0) {
+    rc = plan_impl(p, nullptr, &num_splits, &chunk);
+    if (rc != DA_OK) return rc;
+  }
+  rc = chunk_for_splits(p, num_splits, &chunk, &eff);
+  if (rc != DA_OK) return rc;
+  return eff > 1 ? 2 : 1;
+}
+
+int decode_attn(const decode_attn_params* p, const void* q, const void* k_cache,
+                const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                void* out, float* lse, int32_t num_splits, void* workspace,
+                size_t workspace_bytes, int32_t* status, void* stream) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  const bool paged = block_table != nullptr;
+  rc = check_paged(p, paged);
+  if (rc != DA_OK) return rc;
+  if (p->batch == 0) return DA_OK;
+  // with max_seq_len == 0 no key is ever read: the caches may be empty
+  const bool no_keys = p->max_seq_len == 0;
+  if (q == nullptr || (!no_keys && (k_cache == nullptr || v_cache == nullptr)) ||
+      seq_lens == nullptr || out == nullptr || lse == nullptr)
+    return DA_ERR_NULL_POINTER;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0 ||
+      (paged && (reinterpret_cast<uintptr_t>(block_table) & 3u) != 0))
+    return DA_ERR_ALIGNMENT;
+  if (!stride_ok(p->q_stride_batch) || !stride_ok(p->q_stride_token) ||
+      !stride_ok(p->q_stride_head) || !stride_ok(p->o_stride_batch) ||
+      !stride_ok(p->o_stride_token) || !stride_ok(p->o_stride_head) ||
+      (!no_keys && (!stride_ok(p->kv_stride_page) || !stride_ok(p->kv_stride_token) ||
+                    !stride_ok(p->kv_stride_head))))
+    return DA_ERR_ALIGNMENT;
+
+  DeviceInfo di;
+  rc = current_device_info(&di);
+  if (rc != DA_OK) return rc;
+  if (di.major * 10 + di.minor < 100) return DA_ERR_NO_DEVICE;
+
+  int32_t chunk = 0, eff = 0;
+  if (num_splits <= 0) {
+    rc = plan_impl(p, nullptr, &num_splits, &chunk);
+    if (rc != DA_OK) return rc;
+  }
+  rc = chunk_for_splits(p, num_splits, &chunk, &eff);
+  if (rc != DA_OK) return rc;
+  size_t need = 0;
+  decode_attn_workspace_bytes(p, num_splits, &need);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return DA_ERR_WORKSPACE;
+
+  CUtensorMap kmap, vmap;
+  std::memset(&kmap, 0, sizeof(kmap));
+  std::memset(&vmap, 0, sizeof(vmap));
+  if (!no_keys) {
+    rc = make_kv_map(&kmap, k_cache, p, paged);
+    if (rc != DA_OK) return rc;
+    rc = make_kv_map(&vmap, v_cache, p, paged);
+    if (rc != DA_OK) return rc;
+  }
+
+  dattn::SplitArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const uint16_t*>(q);
+  a.q_sb = p->q_stride_batch;
+  a.q_st = p->q_stride_token;
+  a.q_sh = p->q_stride_head;
+  a.out = static_cast<uint16_t*>(out);
+  a.o_sb = p->o_stride_batch;
+  a.o_st = p->o_stride_token;
+  a.o_sh = p->o_stride_head;
+  a.lse = lse;
+  const size_t rows_total = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
+  a.part_o = eff > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = eff > 1 ? a.part_o + rows_total * eff * kHeadDim : nullptr;
+  a.block_table = block_table;
+  a.bt_stride = p->block_table_stride;
+  a.seq_lens = seq_lens;
+  a.status = status;
+  a.batch = p->batch;
+  a.q_len = p->q_len;
+  a.num_q_heads = p->num_q_heads;
+  a.num_kv_heads = p->num_kv_heads;
+  a.group = p->num_q_heads / p->num_kv_heads;
+  a.rows = rows_of(p);
+  a.page_size = paged ? p->page_size : 0;
+  a.num_pages = paged ? p->num_pages : 0;
+  a.paged = paged ? 1 : 0;
+  a.max_seq_len = p->max_seq_len;
+  a.chunk_len = chunk;
+  a.num_splits = eff;
+  a.causal = p->causal ? 1 : 0;
+  a.scale_log2 = p->scale * 1.4426950408889634f;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dattn::launch_split(kmap, vmap, a, st) != cudaSuccess) return DA_ERR_CUDA;
+  if (eff > 1) {
+    dattn::CombineArgs c;
+    c.part_o = a.part_o;
+    c.part_lse = a.part_lse;
+    c.seq_lens = seq_lens;
+    c.out = a.out;
+    c.o_sb = a.o_sb;
+    c.o_st = a.o_st;
+    c.o_sh = a.o_sh;
+    c.lse = lse;
+    c.batch = p->batch;
+    c.q_len = p->q_len;
+    c.num_q_heads = p->num_q_heads;
+    c.max_seq_len = p->max_seq_len;
+    c.chunk_len = chunk;
+    c.num_splits = eff;
+    if (dattn::launch_combine(c, st) != cudaSuccess) return DA_ERR_CUDA;
+  }
+  return DA_OK;
+}
+
+int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens, int32_t num_splits,
+                        int32_t chunk_len, const void* workspace, size_t workspace_bytes,
+                        void* out, float* lse, void* stream) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (p->batch == 0) return DA_OK;
+  if (seq_lens == nullptr || out == nullptr || lse == nullptr) return DA_ERR_NULL_POINTER;
+  if (num_splits < 1 || chunk_len < 1 || chunk_len % kTileTokens != 0 ||
+      ceil_div64(std::max(p->max_seq_len, 1), chunk_len) > num_splits)
+    return DA_ERR_SPLITS;
+  if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
+      !stride_ok(p->o_stride_batch) || !stride_ok(p->o_stride_token) ||
+      !stride_ok(p->o_stride_head))
+    return DA_ERR_ALIGNMENT;
+  const size_t rows_total = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
+  const size_t need = rows_total * static_cast<size_t>(num_splits) * (kHeadDim + 1) * sizeof(float);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return DA_ERR_WORKSPACE;
+  dattn::CombineArgs c;
+  c.part_o = static_cast<const float*>(workspace);
+  c.part_lse = c.part_o + rows_total * num_splits * kHeadDim;
+  c.seq_lens = seq_lens;
+  c.out = static_cast<uint16_t*>(out);
+  c.o_sb = p->o_stride_batch;
+  c.o_st = p->o_stride_token;
+  c.o_sh = p->o_stride_head;
+  c.lse = lse;
+  c.batch = p->batch;
+  c.q_len = p->q_len;
+  c.num_q_heads = p->num_q_heads;
+  c.max_seq_len = p->max_seq_len;
+  c.chunk_len = chunk_len;
+  c.num_splits = num_splits;
+  if (dattn::launch_combine(c, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+const char* decode_attn_status_string(int code) {
+  switch (code) {
+    case DA_OK: return "ok";
+    case DA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case DA_ERR_BAD_SHAPE: return "invalid sizes (batch, heads, q_len, lengths or paging)";
+    case DA_ERR_HEAD_DIM: return "head_dim must be 128";
+    case DA_ERR_PAGE_SIZE: return "page_size must be a positive multiple of 16";
+    case DA_ERR_ROWS: return "(num_q_heads / num_kv_heads) * q_len exceeds 16";
+    case DA_ERR_ALIGNMENT: return "pointer or stride misaligned (16-byte bases, strides multiple of 8 elements)";
+    case DA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case DA_ERR_NO_DEVICE: return "no usable sm_100-class device is current";
+    case DA_ERR_SPLITS: return "num_splits / chunk_len out of range";
+    default: return "unknown status code";
+  }
+}
+
+}  // extern "C"

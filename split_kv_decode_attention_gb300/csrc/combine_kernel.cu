@@ -1,0 +1,85 @@
+// combine_kernel.cu -- the cross-chunk reduce of split-KV decode attention.
+//
+// For each output row (request b, token t, query head h) whose request spans
+// n >= 2 chunks, merge the normalised fp32 partials O_s and their natural-log
+// LSEs lse_s exactly ("Capstone FlashAttention", §1.2 merge of running max and
+// running sum, applied to all chunks at once; §2.3 FlashDecoding's small
+// cross-SM reduce kernel):
+//     M = max_s lse_s,  w_s = exp(lse_s - M),
+//     out = sum_s w_s O_s / sum_s w_s,   lse = M + ln(sum_s w_s).
+// One warp per row: lane i owns d = 4i..4i+3, so each partial row is one
+// coalesced 512-byte read.  Empty chunks (lse -inf) weigh nothing; a row with
+// no finite lse gives out = 0, lse = -inf.
+
+#include "decode_attn.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace dattn {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const CombineArgs a) {
+  constexpr uint32_t kFull = 0xffffffffu;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
+  const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.num_q_heads;
+  if (row >= nrows) return;
+  const int h = static_cast<int>(row % a.num_q_heads);
+  const int t = static_cast<int>((row / a.num_q_heads) % a.q_len);
+  const int b = static_cast<int>(row / (static_cast<int64_t>(a.num_q_heads) * a.q_len));
+  int L = a.seq_lens[b];
+  L = L < 0 ? 0 : (L > a.max_seq_len ? a.max_seq_len : L);
+  const int n = L > 0 ? (L + a.chunk_len - 1) / a.chunk_len : 1;
+  if (n < 2) return;  // the split kernel wrote this row directly
+
+  const int S = a.num_splits;
+  const float* pl = a.part_lse + row * S;
+  const float* po = a.part_o + row * S * kHeadDim + lane * 4;
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
+  M = fmaxf(M, __shfl_xor_sync(kFull, M, 16));
+  M = fmaxf(M, __shfl_xor_sync(kFull, M, 8));
+  M = fmaxf(M, __shfl_xor_sync(kFull, M, 4));
+  M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
+  M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
+
+  uint16_t* orow = a.out + static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(t) * a.o_st +
+                   static_cast<int64_t>(h) * a.o_sh + lane * 4;
+  if (M == -INFINITY) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+    if (lane == 0) a.lse[row] = -INFINITY;
+    return;
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float W = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < n; ++s) {
+    const float w = ex2((pl[s] - M) * kLog2e);
+    const float4 v = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * kHeadDim);
+    W += w;
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  const float inv = 1.f / W;
+  *reinterpret_cast<uint2*>(orow) =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (lane == 0) a.lse[row] = M + logf(W);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
+  const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.num_q_heads;
+  if (nrows == 0) return cudaSuccess;
+  const int64_t blocks = (nrows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  combine_kernel<<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dattn

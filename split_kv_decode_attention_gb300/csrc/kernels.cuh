@@ -1,0 +1,56 @@
+// kernels.cuh -- internal interface between the C ABI (api.cu) and the
+// decode-attention kernels.  Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dattn {
+
+constexpr int kHeadDim = 128;
+constexpr int kTileTokens = 16;        // tokens per TMA box / per MMA tile
+constexpr int kMaxRows = 16;           // GQA group x q_len rows per CTA
+
+// Arguments of the split kernel (one CTA per (chunk, kv head, request)).
+struct SplitArgs {
+  const uint16_t* q;                   // bf16 [B, q_len, Hq, D]
+  int64_t q_sb, q_st, q_sh;
+  uint16_t* out;                       // bf16 [B, q_len, Hq, D]
+  int64_t o_sb, o_st, o_sh;
+  float* lse;                          // fp32 [B, q_len, Hq]
+  float* part_o;                       // fp32 [B, q_len, Hq, S, D] (S > 1)
+  float* part_lse;                     // fp32 [B, q_len, Hq, S]
+  const int32_t* block_table;          // paged only
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  int32_t* status;                     // optional
+  int batch, q_len, num_q_heads, num_kv_heads, group, rows;
+  int page_size, num_pages, paged;
+  int max_seq_len, chunk_len, num_splits;
+  int causal;
+  float scale_log2;                    // softmax scale * log2(e)
+};
+
+struct CombineArgs {
+  const float* part_o;
+  const float* part_lse;
+  const int32_t* seq_lens;
+  uint16_t* out;
+  int64_t o_sb, o_st, o_sh;
+  float* lse;
+  int batch, q_len, num_q_heads;
+  int max_seq_len, chunk_len, num_splits;
+};
+
+// Launch the split kernel over grid (num_splits, Hkv, B).
+cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
+                         cudaStream_t stream);
+
+// Resident split CTAs per SM for the kernel variant serving `rows` rows.
+int split_ctas_per_sm(int rows);
+
+// Launch the combine kernel (one warp per output row).
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+}  // namespace dattn

@@ -191,7 +191,7 @@ def contiguous_block_table(seq_lens: np.ndarray, page_size: int, max_pages: int)
 def _cache_dims(shape: DecodeShape, seq_lens: np.ndarray):
     max_seq_len = int(seq_lens.max()) if len(seq_lens) else 0
     if shape.paged:
-        max_pages = max(1, -(-shape.seq_len_hi // shape.page_size))
+        max_pages = max(1, -(-max(shape.seq_len_hi, max_seq_len) // shape.page_size))
         return max_seq_len, max_pages
     return max_seq_len, 0
 

@@ -1,0 +1,105 @@
+"""GPU parity of the CUDA path against the fp64 oracle (small and ragged cases).
+
+Every call goes through the C ABI (ctypes binding).  Sizes span several
+16-token tiles, several 64-token pipeline stages and several chunks, with
+ragged tails; the tolerance rule is in tests/parity.py.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from split_kv_decode_attention_gb300 import workloads as W
+from tests.parity import (assert_lse_close, assert_out_close, bf16_tensor_to_bits,
+                          bf16_tensor_to_f64, to_device)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def binding():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from split_kv_decode_attention_gb300 import binding as B
+    from split_kv_decode_attention_gb300 import build as cuda_build
+    cuda_build.build()
+    B.lib()
+    return B
+
+
+def run(binding, inp, num_splits=0, status=None, **kw):
+    q, k, v, bt, lens = to_device(inp)
+    out, lse = binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len,
+                                   causal=inp.shape.causal, scale=inp.shape.scale,
+                                   num_splits=num_splits, status=status, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check(binding, inp, num_splits=0):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run(binding, inp, num_splits, status=status)
+    ref_o, ref_l = oracle.decode_attention_inputs(inp)
+    assert int(status.item()) == 0
+    assert_out_close(bf16_tensor_to_f64(out), ref_o)
+    assert_lse_close(lse.cpu().numpy(), ref_l)
+    return out, lse
+
+
+CASES = [
+    # name, G, q_len, causal, paged, page_size, lo, hi
+    ("mha_contig", 1, 1, False, False, 16, 1, 700),
+    ("gqa4_paged", 4, 1, False, True, 16, 1, 900),
+    ("gqa8_paged_peaked", 8, 1, False, True, 16, 100, 1200),
+    ("gqa4_q4_causal", 4, 4, True, True, 16, 4, 800),
+    ("gqa4_q4_nocausal", 4, 4, False, True, 16, 4, 600),
+    ("gqa2_q3_causal_contig", 2, 3, True, False, 16, 3, 500),
+    ("gqa16_paged", 16, 1, False, True, 16, 1, 400),
+    ("mha_q16_causal", 1, 16, True, True, 16, 16, 300),
+    ("gqa4_q2_page32", 4, 2, True, True, 32, 2, 700),
+    ("gqa8_page64", 8, 1, False, True, 64, 1, 500),
+]
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_small_workloads_match_oracle(binding, case, splits):
+    name, G, T, causal, paged, ps, lo, hi = case
+    shp = W.small_shape(name, batch=4, q_len=T, num_q_heads=2 * G, num_kv_heads=2,
+                        lo=lo, hi=hi, paged=paged, page_size=ps, causal=causal,
+                        peaked=0.05 if "peaked" in name else 0.0, seed=100 + G + T)
+    inp = W.make_host_inputs(shp)
+    check(binding, inp, splits)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_edge_lengths_including_empty_requests(binding, splits):
+    lens = np.array([0, 1, 15, 16, 17, 63, 64, 65, 127, 129, 0, 250], np.int32)
+    shp = W.small_shape("edges", batch=len(lens), num_q_heads=8, num_kv_heads=2,
+                        lo=0, hi=256, paged=True, seed=31)
+    inp = W.make_host_inputs(shp, seq_lens=lens)
+    out, lse = check(binding, inp, splits)
+    o = bf16_tensor_to_f64(out)
+    assert np.all(o[0] == 0) and np.all(o[10] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[[0, 10]]))
+
+
+def test_all_requests_empty(binding):
+    shp = W.small_shape("empty", batch=3, num_q_heads=4, num_kv_heads=1, lo=0, hi=0,
+                        paged=False, seed=32)
+    inp = W.make_host_inputs(shp, seq_lens=np.zeros(3, np.int32))
+    q, _, _, _, lens = to_device(inp)
+    # contiguous cache with max_seq_len = 0: caches may be empty
+    k = torch.empty((3, 0, 1, 128), dtype=torch.bfloat16, device="cuda")
+    out, lse = binding.decode_attn(q, k, k, None, lens, max_seq_len=0, num_splits=1)
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 0)
+    assert torch.all(torch.isneginf(lse))
+
+
+def test_long_single_request_many_splits(binding):
+    shp = W.small_shape("long", batch=1, num_q_heads=4, num_kv_heads=1, lo=20011,
+                        hi=20011, paged=False, seed=33)
+    inp = W.make_host_inputs(shp)
+    for s in (1, 5, 40, 0):
+        check(binding, inp, s)
