@@ -179,6 +179,20 @@ int decode_attn(const decode_attn_params *p, const void *q, const void *k_cache,
                 int32_t *status, void *stream);
 
 /*
+ * The split pass alone: the same arguments and the same first launch as
+ * decode_attn().  Rows of requests that fit one chunk get their final out/lse;
+ * rows of longer requests get partials in `workspace` (layout above), which
+ * decode_attn_combine() with the same num_splits and the chunk length from
+ * decode_attn_chunk_len() then merges.  decode_attn() == decode_attn_split()
+ * followed by decode_attn_combine().
+ */
+int decode_attn_split(const decode_attn_params *p, const void *q, const void *k_cache,
+                      const void *v_cache, const int32_t *block_table,
+                      const int32_t *seq_lens, void *out, float *lse,
+                      int32_t num_splits, void *workspace, size_t workspace_bytes,
+                      int32_t *status, void *stream);
+
+/*
  * The combine step alone: merges the partials that a split pass left in
  * `workspace` (layout above) into out/lse, for every row whose request uses
  * two or more chunks of `chunk_len` tokens.  M = max_s lse_s,

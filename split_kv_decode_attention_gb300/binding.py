@@ -27,7 +27,7 @@ DA_STATUS_TIMEOUT = 8
 
 EXPORTED_SYMBOLS = (
     "decode_attn_params_init", "decode_attn_plan", "decode_attn_chunk_len",
-    "decode_attn_workspace_bytes", "decode_attn", "decode_attn_combine",
+    "decode_attn_workspace_bytes", "decode_attn", "decode_attn_split", "decode_attn_combine",
     "decode_attn_status_string", "decode_attn_launch_count",
 )
 
@@ -77,12 +77,14 @@ def lib() -> ctypes.CDLL:
         L.decode_attn_chunk_len.argtypes = [P, i32, pi32]
         L.decode_attn_workspace_bytes.argtypes = [P, i32, ctypes.POINTER(sz)]
         L.decode_attn.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp, vp]
+        L.decode_attn_split.argtypes = L.decode_attn.argtypes
         L.decode_attn_combine.argtypes = [P, vp, i32, i32, vp, sz, vp, vp, vp]
         L.decode_attn_status_string.argtypes = [ctypes.c_int]
         L.decode_attn_status_string.restype = ctypes.c_char_p
         L.decode_attn_launch_count.argtypes = [P, i32]
         for f in ("decode_attn_plan", "decode_attn_chunk_len", "decode_attn_workspace_bytes",
-                  "decode_attn", "decode_attn_combine", "decode_attn_launch_count"):
+                  "decode_attn", "decode_attn_split", "decode_attn_combine",
+                  "decode_attn_launch_count"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -228,3 +230,16 @@ def workspace_views(workspace, p: DecodeAttnParams, num_splits: int):
     po = f[: rows * S * HEAD_DIM].view(p.batch, p.q_len, p.num_q_heads, S, HEAD_DIM)
     pl = f[rows * S * HEAD_DIM:].view(p.batch, p.q_len, p.num_q_heads, S)
     return po, pl
+
+
+def decode_attn_split(p: DecodeAttnParams, q, k_cache, v_cache, block_table, seq_lens, out,
+                      lse, num_splits: int, workspace=None, status=None, stream=None):
+    """The split pass alone (same arguments as the C entry point): final
+    out/lse for requests that fit one chunk, partials in `workspace` for the
+    rest; decode_attn_combine() with the same num_splits finishes them."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().decode_attn_split(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse),
+                                   int(num_splits), _ptr(workspace), ws_bytes, _ptr(status),
+                                   _stream_handle(stream)), "decode_attn_split")
+    return out, lse

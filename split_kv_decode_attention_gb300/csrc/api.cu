@@ -245,10 +245,15 @@ int decode_attn_launch_count(const decode_attn_params* p, int32_t num_splits) {
   return eff > 1 ? 2 : 1;
 }
 
-int decode_attn(const decode_attn_params* p, const void* q, const void* k_cache,
-                const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
-                void* out, float* lse, int32_t num_splits, void* workspace,
-                size_t workspace_bytes, int32_t* status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The whole path (run_combine) or the split pass alone.
+int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
+               const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+               void* out, float* lse, int32_t num_splits, void* workspace,
+               size_t workspace_bytes, int32_t* status, void* stream, bool run_combine) {
   int rc = check_shape(p);
   if (rc != DA_OK) return rc;
   const bool paged = block_table != nullptr;
@@ -334,7 +339,7 @@ int decode_attn(const decode_attn_params* p, const void* q, const void* k_cache,
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dattn::launch_split(kmap, vmap, a, st) != cudaSuccess) return DA_ERR_CUDA;
-  if (eff > 1) {
+  if (run_combine && eff > 1) {
     dattn::CombineArgs c;
     c.part_o = a.part_o;
     c.part_lse = a.part_lse;
@@ -353,6 +358,26 @@ int decode_attn(const decode_attn_params* p, const void* q, const void* k_cache,
     if (dattn::launch_combine(c, st) != cudaSuccess) return DA_ERR_CUDA;
   }
   return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int decode_attn(const decode_attn_params* p, const void* q, const void* k_cache,
+                const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                void* out, float* lse, int32_t num_splits, void* workspace,
+                size_t workspace_bytes, int32_t* status, void* stream) {
+  return run_decode(p, q, k_cache, v_cache, block_table, seq_lens, out, lse, num_splits,
+                    workspace, workspace_bytes, status, stream, true);
+}
+
+int decode_attn_split(const decode_attn_params* p, const void* q, const void* k_cache,
+                      const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                      void* out, float* lse, int32_t num_splits, void* workspace,
+                      size_t workspace_bytes, int32_t* status, void* stream) {
+  return run_decode(p, q, k_cache, v_cache, block_table, seq_lens, out, lse, num_splits,
+                    workspace, workspace_bytes, status, stream, false);
 }
 
 int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens, int32_t num_splits,
