@@ -1,0 +1,51 @@
+"""The benchmark's multi-process (replica) logic on CPU with gloo, world size 2:
+rank setup from the torchrun environment, barrier, and max-over-ranks of the
+step time that rank 0 reports."""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update({"RANK": str(rank), "LOCAL_RANK": str(rank), "WORLD_SIZE": str(world),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import bench
+    d = bench.Dist(backend="gloo")
+    d.barrier()
+    ms = 1.0 + rank * 2.5          # rank 1 is the slow one
+    m = d.max(ms)
+    d.barrier()
+    q.put((rank, d.world, m))
+    d.close()
+
+
+def test_two_ranks_agree_on_max_step_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2, 3.5), (1, 2, 3.5)]
+
+
+def test_single_process_needs_no_process_group(monkeypatch):
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    import bench
+    d = bench.Dist()
+    assert d.world == 1 and d.rank == 0 and d.pg is None
+    assert d.max(4.0) == 4.0
