@@ -76,6 +76,10 @@ extern "C" {
 #define DA_ERR_CUDA -8             /* a CUDA runtime call or launch failed */
 #define DA_ERR_NO_DEVICE -9        /* no usable sm_103 device is current */
 #define DA_ERR_SPLITS -10          /* num_splits out of range */
+#define DA_ERR_STATIC_WORKSPACE_LIMIT -11 /* partials exceed the static workspace */
+
+/* size of the device array behind decode_attn_static_workspace() */
+#define DECODE_ATTN_STATIC_WORKSPACE_BYTES (16u << 20)
 
 /* device status bits (OR-ed into *status) */
 #define DA_STATUS_BAD_PAGE 1u      /* block-table entry outside [0, num_pages) */
@@ -205,6 +209,30 @@ int decode_attn_combine(const decode_attn_params *p, const int32_t *seq_lens,
                         int32_t num_splits, int32_t chunk_len,
                         const void *workspace, size_t workspace_bytes, void *out,
                         float *lse, void *stream);
+
+/*
+ * decode_attn() for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this entry point; it exists for callers such as
+ * plugin hosts that pass only input and output buffers, runtimes whose device
+ * memory is owned by another allocator, and deployments that forbid device
+ * allocation after start-up.  Same arguments as decode_attn() minus the
+ * workspace: the partials go to a DECODE_ATTN_STATIC_WORKSPACE_BYTES (16 MiB)
+ * array in the library's own device memory, which every GPU that loads the
+ * library holds until the process exits.
+ *   - A call needing more than that returns DA_ERR_STATIC_WORKSPACE_LIMIT and
+ *     launches nothing (decode_attn_workspace_bytes() gives the need).
+ *   - All calls on a device share the array, and it keeps the last call's
+ *     contents (nothing in it needs clearing).  Calls that overlap on the GPU
+ *     race on it: serialise them.
+ *   - The first call on each device looks up the array's address with that
+ *     device current; make it before any stream capture on that device.
+ * Allocates nothing (no cudaMalloc/cudaFree or allocating library call).
+ */
+int decode_attn_static_workspace(const decode_attn_params *p, const void *q,
+                                 const void *k_cache, const void *v_cache,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 void *out, float *lse, int32_t num_splits,
+                                 int32_t *status, void *stream);
 
 /* Static description of a return code. */
 const char *decode_attn_status_string(int code);

@@ -28,8 +28,10 @@ DA_STATUS_TIMEOUT = 8
 EXPORTED_SYMBOLS = (
     "decode_attn_params_init", "decode_attn_plan", "decode_attn_chunk_len",
     "decode_attn_workspace_bytes", "decode_attn", "decode_attn_split", "decode_attn_combine",
-    "decode_attn_status_string", "decode_attn_launch_count",
+    "decode_attn_status_string", "decode_attn_launch_count", "decode_attn_static_workspace",
 )
+DA_ERR_STATIC_WORKSPACE_LIMIT = -11
+STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class DecodeAttnParams(ctypes.Structure):
@@ -78,13 +80,14 @@ def lib() -> ctypes.CDLL:
         L.decode_attn_workspace_bytes.argtypes = [P, i32, ctypes.POINTER(sz)]
         L.decode_attn.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp, vp]
         L.decode_attn_split.argtypes = L.decode_attn.argtypes
+        L.decode_attn_static_workspace.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp]
         L.decode_attn_combine.argtypes = [P, vp, i32, i32, vp, sz, vp, vp, vp]
         L.decode_attn_status_string.argtypes = [ctypes.c_int]
         L.decode_attn_status_string.restype = ctypes.c_char_p
         L.decode_attn_launch_count.argtypes = [P, i32]
         for f in ("decode_attn_plan", "decode_attn_chunk_len", "decode_attn_workspace_bytes",
                   "decode_attn", "decode_attn_split", "decode_attn_combine",
-                  "decode_attn_launch_count"):
+                  "decode_attn_launch_count", "decode_attn_static_workspace"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -242,4 +245,18 @@ def decode_attn_split(p: DecodeAttnParams, q, k_cache, v_cache, block_table, seq
                                    _ptr(block_table), _ptr(seq_lens), _ptr(out), _ptr(lse),
                                    int(num_splits), _ptr(workspace), ws_bytes, _ptr(status),
                                    _stream_handle(stream)), "decode_attn_split")
+    return out, lse
+
+
+def decode_attn_static_workspace(p: DecodeAttnParams, q, k_cache, v_cache, block_table,
+                                 seq_lens, out, lse, num_splits: int = 0, status=None,
+                                 stream=None):
+    """decode_attn() without a caller workspace, for callers that cannot
+    allocate device memory: the partials live in the library's fixed 16 MiB
+    device array (shared by all calls on a device; overlapping calls race).
+    Raises DecodeAttnError(-11) when a call needs more than that."""
+    _check(lib().decode_attn_static_workspace(
+        ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(out), _ptr(lse), int(num_splits), _ptr(status),
+        _stream_handle(stream)), "decode_attn_static_workspace")
     return out, lse

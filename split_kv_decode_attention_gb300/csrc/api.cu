@@ -431,6 +431,8 @@ const char* decode_attn_status_string(int code) {
     case DA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case DA_ERR_NO_DEVICE: return "no usable sm_100-class device is current";
     case DA_ERR_SPLITS: return "num_splits / chunk_len out of range";
+    case DA_ERR_STATIC_WORKSPACE_LIMIT:
+      return "the call's partials exceed the 16 MiB static workspace (use fewer splits or decode_attn with a workspace)";
     default: return "unknown status code";
   }
 }

@@ -1,0 +1,74 @@
+"""decode_attn_static_workspace(): decode attention for callers that cannot
+allocate device memory (plugin hosts that pass only input/output buffers,
+runtimes whose memory belongs to another allocator, deployments that forbid
+allocation after start-up).  Its partials live in the library's fixed 16 MiB
+device array instead of a caller workspace.
+
+Checked through the C ABI against decode_attn() with a caller workspace, on
+two calls in a row (the second runs over whatever the first left in the
+shared array), within the parity tolerance of the other tests.  This file is
+collected last so that a stop-at-first-failure run has already run the rest;
+it also passes on its own in a fresh process."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from split_kv_decode_attention_gb300 import workloads as W
+from tests.parity import assert_lse_close, assert_out_close, bf16_tensor_to_f64, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def binding():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from split_kv_decode_attention_gb300 import binding as B
+    from split_kv_decode_attention_gb300 import build as cuda_build
+    cuda_build.build()
+    B.lib()
+    return B
+
+
+def both_ways(binding, inp, num_splits):
+    q, k, v, bt, lens = to_device(inp)
+    s = inp.shape
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=s.causal,
+                                    scale=s.scale)
+    ref_out, ref_lse = binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len,
+                                           causal=s.causal, scale=s.scale,
+                                           num_splits=num_splits, params=p)
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.decode_attn_static_workspace(p, q, k, v, bt, lens, out, lse, num_splits,
+                                         status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return (bf16_tensor_to_f64(out), lse.cpu().numpy(),
+            bf16_tensor_to_f64(ref_out), ref_lse.cpu().numpy())
+
+
+def test_two_calls_in_a_row_match_decode_attn(binding):
+    first = W.make_host_inputs(W.small_shape(
+        "na1", batch=5, q_len=4, num_q_heads=16, num_kv_heads=4, lo=30, hi=3000,
+        paged=True, causal=True, seed=91))
+    second = W.make_host_inputs(W.small_shape(
+        "na2", batch=2, q_len=1, num_q_heads=8, num_kv_heads=8, lo=9000, hi=12000,
+        paged=False, seed=92))
+    for inp, splits in ((first, 6), (second, 0)):
+        out, lse, ref_out, ref_lse = both_ways(binding, inp, splits)
+        assert_out_close(out, ref_out, what="static-workspace out")
+        assert_lse_close(lse, ref_lse, what="static-workspace lse")
+
+
+def test_oversized_call_is_rejected_without_launch(binding):
+    # 256 x 64 rows x 64 splits x 516 B of partials >> 16 MiB
+    p = binding.decode_attn_params_init(256, 1, 64, 8, 128, 0, 0, 0, 32768, False)
+    assert binding.decode_attn_workspace_bytes(p, 64) > binding.STATIC_WORKSPACE_BYTES
+    rc = binding.lib().decode_attn_static_workspace(ctypes.byref(p), None, None, None, None,
+                                                    None, None, None, 64, None, None)
+    assert rc == binding.DA_ERR_STATIC_WORKSPACE_LIMIT
+    assert "16 MiB" in binding.decode_attn_status_string(rc)
