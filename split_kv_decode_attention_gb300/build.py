@@ -40,9 +40,9 @@ def _deps():
         [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, extra=(), build_dir=BUILD_DIR) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -53,24 +53,28 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile csrc/*.cu and link lib/libdecode_attn.so; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    os.makedirs(LIB_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB_PATH):
+def build(force: bool = False, verbose_ptxas: bool = False, extra_flags=(),
+          lib_path: str = LIB_PATH) -> str:
+    """Compile csrc/*.cu and link lib/libdecode_attn.so (or `lib_path`, with
+    `extra_flags` such as -D overrides of the pipeline shape); returns its path."""
+    build_dir = BUILD_DIR if lib_path == LIB_PATH else os.path.dirname(lib_path) + "/_obj"
+    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
+    if not force and os.path.exists(lib_path):
         newest = max(os.path.getmtime(p) for p in _deps())
-        if os.path.getmtime(LIB_PATH) >= newest:
-            return LIB_PATH
+        if os.path.getmtime(lib_path) >= newest:
+            return lib_path
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, tuple(extra_flags), build_dir),
+                           srcs))
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -23,6 +23,11 @@ constexpr int kMaxDevices = 64;
 // Planner: a chunk is never shorter than this many tokens (partials and the
 // combine cost ~1.5 KB per row per chunk; a 16 KB+ chunk read keeps that small).
 constexpr int kMinChunkTokens = 256;
+// Ragged batches: chunks are sized for this many waves of resident CTAs over
+// the batch's total work, and hold at least kTokensPerRow tokens per query row
+// (fit on GB300 sweeps of chunk length: ~1-2K tokens for 4-16 rows).
+constexpr int kRaggedWaves = 8;
+constexpr int kTokensPerRow = 64;
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -113,25 +118,34 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
   DeviceInfo di;
   int rc = current_device_info(&di);
   if (rc != DA_OK) return rc;
+  const int rows = rows_of(p);
   const int64_t max_tiles = ceil_div64(std::max(p->max_seq_len, 1), kTileTokens);
   const int64_t pairs = static_cast<int64_t>(std::max(p->batch, 1)) * p->num_kv_heads;
-  const int64_t slots = static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows_of(p));
-  int64_t splits = 1;
-  if (host_seq_lens == nullptr) {
-    // uniform lengths: one wave of equal chunks -- as many chunks per
-    // (request, kv head) as fit the resident CTA slots
-    if (pairs < slots) splits = slots / pairs;
-  } else {
-    // ragged lengths: aim at ~2 waves of chunks over the actual work so the
-    // long requests are cut into pieces comparable to the short ones
-    int64_t work_tiles = 0;
+  const int64_t slots = static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows);
+  bool uniform = true;
+  int64_t work_tokens = 0;
+  if (host_seq_lens != nullptr) {
     for (int32_t b = 0; b < p->batch; ++b) {
       const int64_t Lb = std::min<int64_t>(std::max(host_seq_lens[b], 0), p->max_seq_len);
-      work_tiles += ceil_div64(Lb, kTileTokens);
+      work_tokens += Lb;
+      if (host_seq_lens[b] != host_seq_lens[0]) uniform = false;
     }
-    work_tiles *= p->num_kv_heads;
-    const int64_t target_tiles = std::max<int64_t>(1, ceil_div64(work_tiles, 2 * slots));
-    splits = ceil_div64(max_tiles, target_tiles);
+  }
+  int64_t splits = 1;
+  int64_t min_chunk = kMinChunkTokens;
+  if (uniform) {
+    // equal lengths: one full wave of equal chunks -- as many chunks per
+    // (request, kv head) as there are resident CTA slots for them
+    if (pairs < slots) splits = slots / pairs;
+  } else {
+    // ragged lengths: ~kRaggedWaves waves of chunks over the actual work, so
+    // long requests are cut into pieces that keep the tail short; a chunk
+    // costs rows x 516 B of partials written and read back, so chunks grow
+    // with the row count (kTokensPerRow tokens per query row at least)
+    const int64_t per_cta = ceil_div64(work_tokens * p->num_kv_heads, kRaggedWaves * slots);
+    min_chunk = std::max<int64_t>(kMinChunkTokens, static_cast<int64_t>(kTokensPerRow) * rows);
+    const int64_t target = std::max<int64_t>(min_chunk, per_cta);
+    splits = ceil_div64(std::max(p->max_seq_len, 1), target);
   }
   splits = std::min<int64_t>(splits, std::max<int64_t>(1, p->max_seq_len / kMinChunkTokens));
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, max_tiles));

@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const Comb
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
+  // the split kernel that wrote the partials may still be running (this
+  // kernel may launch during its tail): wait before reading anything
+  grid_dependency_wait();
   const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.num_q_heads;
   if (row >= nrows) return;
   const int h = static_cast<int>(row % a.num_q_heads);
@@ -39,6 +42,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const Comb
   const int S = a.num_splits;
   const float* pl = a.part_lse + row * S;
   const float* po = a.part_o + row * S * kHeadDim + lane * 4;
+  // lane i holds lse of splits i, i + 32, ...; the row max by warp shuffles
   float M = -INFINITY;
   for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 16));
@@ -56,15 +60,29 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const Comb
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float W = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < n; ++s) {
-    const float w = ex2((pl[s] - M) * kLog2e);
-    const float4 v = *reinterpret_cast<const float4*>(po + static_cast<int64_t>(s) * kHeadDim);
-    W += w;
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
+  // splits in groups of 32: lane j owns the weight of split s0 + j; each lane
+  // then streams the group's partial rows, kBatch loads in flight at a time
+  constexpr int kBatch = 8;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    const int cnt = min(32, n - s0);
+    const float w_mine = lane < cnt ? ex2((pl[s0 + lane] - M) * kLog2e) : 0.f;
+    for (int j0 = 0; j0 < cnt; j0 += kBatch) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        v[j] = j0 + j < cnt ? *reinterpret_cast<const float4*>(
+                                  po + static_cast<int64_t>(s0 + j0 + j) * kHeadDim)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float w = __shfl_sync(kFull, w_mine, (j0 + j) & 31);
+        W += w;
+        acc.x += w * v[j].x;
+        acc.y += w * v[j].y;
+        acc.z += w * v[j].z;
+        acc.w += w * v[j].w;
+      }
+    }
   }
   const float inv = 1.f / W;
   *reinterpret_cast<uint2*>(orow) =
@@ -78,8 +96,16 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.num_q_heads;
   if (nrows == 0) return cudaSuccess;
   const int64_t blocks = (nrows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  combine_kernel<<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(32 * kWarpsPerBlock);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace dattn

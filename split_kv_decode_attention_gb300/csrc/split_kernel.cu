@@ -81,6 +81,10 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // launched early behind the previous kernel of the stream: nothing that
+  // kernel may write (q, caches, lengths, outputs) is touched before this
+  grid_dependency_wait();
+
   // ---- this CTA's key range [t_begin, t_end)
   int L = a.seq_lens[b];
   uint32_t bad = 0;
@@ -324,6 +328,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
   if (!ok && lane == 0 && a.status != nullptr)
     atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
 
+  // the main loop is done: the combine kernel may start launching
+  if (threadIdx.x == 0) allow_dependent_launch();
+
   // ---- merge the consumer warps' (m, l, O) with the same recurrence
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -418,10 +425,19 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
   }
 }
 
-// The one pipeline shape used for now: 4 consumer warps (one 16-token tile
-// each per stage, 64 tokens = 32 KB of K+V per stage), 3 stages in flight.
-constexpr int kStages = 3;
-constexpr int kTilesPerStage = 4;
+// Pipeline shape: kTilesPerStage consumer warps (one 16-token tile each per
+// stage; 2 tiles = 32 tokens = 16 KB of K+V per stage), kStages stages in
+// flight (48 KB of shared memory, 4 CTAs per SM).  Chosen by GB300 sweeps over
+// (stages, tiles): shapes with 2-3 CTAs per SM beat one large CTA per SM by
+// 1.5-2x on ragged paged batches.  Overridable at build time for sweeps.
+#ifndef DATTN_STAGES
+#define DATTN_STAGES 3
+#endif
+#ifndef DATTN_TILES_PER_STAGE
+#define DATTN_TILES_PER_STAGE 2
+#endif
+constexpr int kStages = DATTN_STAGES;
+constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
 
 template <int NT>
 struct Variant {
@@ -453,9 +469,17 @@ cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitA
                       cudaStream_t st) {
   cudaError_t e = ensure_attrs<NT>();
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-  Variant<NT>::kernel<<<grid, Variant<NT>::C::kThreads, Variant<NT>::C::kSmemBytes, st>>>(km, vm, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_splits, a.num_kv_heads, a.batch);
+  cfg.blockDim = dim3(Variant<NT>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT>::C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, Variant<NT>::kernel, km, vm, a);
 }
 
 template <int NT>
