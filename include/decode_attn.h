@@ -22,7 +22,11 @@
  * writes an fp32 partial output plus its log-sum-exp; a combine kernel merges
  * the partials exactly ("Capstone FlashAttention", §2.3 FlashDecoding; the
  * per-tile LSE buffer of the CUTLASS split-KV post, §4.2).  Requests whose
- * keys fit one chunk skip the partials and the combine.
+ * keys fit one chunk skip the partials and the combine.  When the call needs
+ * 2..16 chunks per (request, kv head) and all of them fit on the GPU at once,
+ * the chunks of one head run as a thread-block cluster and merge through
+ * distributed shared memory instead: one launch, no partials in memory (the
+ * workspace is then unused; DA_FLAG_TWO_PASS turns this off).
  *
  * Cache layouts.  K and V share one layout; head_dim is contiguous.
  *   paged (block_table != NULL): element (page, slot, head, d) of a cache is at
@@ -81,6 +85,11 @@ extern "C" {
 /* size of the device array behind decode_attn_static_workspace() */
 #define DECODE_ATTN_STATIC_WORKSPACE_BYTES (16u << 20)
 
+/* params.flags */
+#define DA_FLAG_TWO_PASS 1u        /* always write fp32 partials to the workspace and
+                                      merge them with the combine kernel (no
+                                      cluster merge); needed to read partials */
+
 /* device status bits (OR-ed into *status) */
 #define DA_STATUS_BAD_PAGE 1u      /* block-table entry outside [0, num_pages) */
 #define DA_STATUS_SEQ_LEN 2u       /* seq_len < 0 or > max_seq_len (clamped) */
@@ -102,7 +111,7 @@ typedef struct decode_attn_params {
                                  request; paged: <= max_pages_per_seq*page_size */
   int32_t causal;             /* nonzero: causal mask among the q_len tokens */
   float scale;                /* softmax scale, e.g. 1/sqrt(head_dim) */
-  int32_t reserved0;          /* must be 0 */
+  int32_t flags;              /* DA_FLAG_* bits; 0 for the default path */
   int64_t q_stride_batch;     /* q [B, q_len, Hq, D] element strides; */
   int64_t q_stride_token;     /*   D contiguous, strides multiples of 8 */
   int64_t q_stride_head;
@@ -149,7 +158,8 @@ int decode_attn_chunk_len(const decode_attn_params *p, int32_t num_splits,
                           int32_t *chunk_len);
 
 /*
- * Workspace bytes decode_attn() needs for num_splits (0 when num_splits == 1).
+ * Workspace bytes decode_attn() needs for num_splits (0 when num_splits == 1;
+ * unused when the cluster merge applies, see above).
  * Layout (fp32): partial outputs [B, q_len, Hq, num_splits, D], followed by
  * partial log-sum-exps [B, q_len, Hq, num_splits] (natural log).  Partial s of
  * a row is normalised (sum of weights 1) over its chunk's keys; an empty
@@ -205,6 +215,9 @@ int decode_attn_split(const decode_attn_params *p, const void *q, const void *k_
  * chunks).  decode_attn() calls it itself; it is exported so that the merge
  * can be run and checked on its own.
  */
+/*   num_splits / chunk_len: the values the split pass used (num_splits ==
+ *   ceil(max_seq_len / chunk_len)).  Launches nothing when that split pass
+ *   merged through clusters (same params, same num_splits). */
 int decode_attn_combine(const decode_attn_params *p, const int32_t *seq_lens,
                         int32_t num_splits, int32_t chunk_len,
                         const void *workspace, size_t workspace_bytes, void *out,
@@ -237,7 +250,8 @@ int decode_attn_static_workspace(const decode_attn_params *p, const void *q,
 /* Static description of a return code. */
 const char *decode_attn_status_string(int code);
 
-/* Number of kernel launches decode_attn() makes for these arguments (1 or 2). */
+/* Number of kernel launches decode_attn() makes for these arguments (1 or 2;
+ * 1 with the cluster merge). */
 int decode_attn_launch_count(const decode_attn_params *p, int32_t num_splits);
 
 #ifdef __cplusplus

@@ -24,6 +24,7 @@ DA_STATUS_BAD_PAGE = 1
 DA_STATUS_SEQ_LEN = 2
 DA_STATUS_SHORT_CAUSAL = 4
 DA_STATUS_TIMEOUT = 8
+DA_FLAG_TWO_PASS = 1
 
 EXPORTED_SYMBOLS = (
     "decode_attn_params_init", "decode_attn_plan", "decode_attn_chunk_len",
@@ -43,7 +44,7 @@ class DecodeAttnParams(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
         ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32),
         ("max_seq_len", ctypes.c_int32), ("causal", ctypes.c_int32),
-        ("scale", ctypes.c_float), ("reserved0", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("flags", ctypes.c_int32),
         ("q_stride_batch", ctypes.c_int64), ("q_stride_token", ctypes.c_int64),
         ("q_stride_head", ctypes.c_int64), ("o_stride_batch", ctypes.c_int64),
         ("o_stride_token", ctypes.c_int64), ("o_stride_head", ctypes.c_int64),
@@ -126,7 +127,7 @@ def decode_attn_params_init(batch: int, q_len: int, num_q_heads: int, num_kv_hea
 
 def params_from_tensors(q, k_cache, block_table=None, *, max_seq_len: int,
                         causal: bool = False, scale: Optional[float] = None,
-                        out=None) -> DecodeAttnParams:
+                        out=None, two_pass: bool = False) -> DecodeAttnParams:
     """Describe torch tensors: q/out [B, q_len, Hq, D]; k_cache paged
     [P, page_size, Hkv, D] (block_table [B, max_pages] given) or contiguous
     [B, S, Hkv, D].  Strides are taken from the tensors."""
@@ -138,6 +139,7 @@ def params_from_tensors(q, k_cache, block_table=None, *, max_seq_len: int,
     p.batch, p.q_len, p.num_q_heads, p.num_kv_heads, p.head_dim = B, T, Hq, Hkv, D
     p.max_seq_len = int(max_seq_len)
     p.causal = 1 if causal else 0
+    p.flags = DA_FLAG_TWO_PASS if two_pass else 0
     p.scale = float(scale if scale is not None else 1.0 / math.sqrt(D))
     p.q_stride_batch, p.q_stride_token, p.q_stride_head = (int(s) for s in q.stride()[:3])
     o = out if out is not None else q
@@ -187,7 +189,7 @@ def decode_attn_launch_count(p: DecodeAttnParams, num_splits: int) -> int:
 def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
                 causal: bool = False, scale: Optional[float] = None, num_splits: int = 0,
                 out=None, lse=None, workspace=None, status=None, stream=None,
-                params: Optional[DecodeAttnParams] = None):
+                params: Optional[DecodeAttnParams] = None, two_pass: bool = False):
     """Run decode attention; returns (out bf16 [B, q_len, Hq, D], lse fp32
     [B, q_len, Hq]).  Output, LSE and workspace tensors are allocated with
     torch when not given; `num_splits <= 0` lets the library's planner choose."""
@@ -199,7 +201,8 @@ def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
     if lse is None:
         lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
     p = params if params is not None else params_from_tensors(
-        q, k_cache, block_table, max_seq_len=max_seq_len, causal=causal, scale=scale, out=out)
+        q, k_cache, block_table, max_seq_len=max_seq_len, causal=causal, scale=scale, out=out,
+        two_pass=two_pass)
     if num_splits <= 0:
         num_splits, _ = decode_attn_plan(p)
     need = decode_attn_workspace_bytes(p, num_splits)

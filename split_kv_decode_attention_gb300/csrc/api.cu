@@ -28,6 +28,8 @@ constexpr int kMinChunkTokens = 256;
 // (fit on GB300 sweeps of chunk length: ~1-2K tokens for 4-16 rows).
 constexpr int kRaggedWaves = 8;
 constexpr int kTokensPerRow = 64;
+// Largest thread-block cluster the split kernel uses (non-portable size).
+constexpr int kMaxClusterSplits = 16;
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -82,7 +84,8 @@ int check_shape(const decode_attn_params* p) {
   if (p == nullptr) return DA_ERR_NULL_POINTER;
   if (p->batch < 0 || p->batch > 65535 || p->q_len < 1 || p->num_q_heads < 1 ||
       p->num_kv_heads < 1 || p->num_kv_heads > 65535 || p->max_seq_len < 0 ||
-      p->num_q_heads % p->num_kv_heads != 0 || p->reserved0 != 0 || !std::isfinite(p->scale))
+      p->num_q_heads % p->num_kv_heads != 0 || (p->flags & ~DA_FLAG_TWO_PASS) != 0 ||
+      !std::isfinite(p->scale))
     return DA_ERR_BAD_SHAPE;
   if (p->head_dim != DECODE_ATTN_HEAD_DIM) return DA_ERR_HEAD_DIM;
   if (static_cast<int64_t>(p->num_q_heads / p->num_kv_heads) * p->q_len > DECODE_ATTN_MAX_ROWS)
@@ -135,8 +138,9 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
   int64_t min_chunk = kMinChunkTokens;
   if (uniform) {
     // equal lengths: one full wave of equal chunks -- as many chunks per
-    // (request, kv head) as there are resident CTA slots for them
-    if (pairs < slots) splits = slots / pairs;
+    // (request, kv head) as there are resident CTA slots for them, at most
+    // kMaxClusterSplits so that the chunks of a head can merge as a cluster
+    if (pairs < slots) splits = std::min<int64_t>(slots / pairs, kMaxClusterSplits);
   } else {
     // ragged lengths: ~kRaggedWaves waves of chunks over the actual work, so
     // long requests are cut into pieces that keep the tail short; a chunk
@@ -179,6 +183,15 @@ int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p,
 }
 
 bool stride_ok(int64_t s) { return s > 0 && s % 8 == 0 && s * 2 < (1LL << 40); }
+
+// The split pass merges through thread-block clusters (no partials, no
+// combine) when allowed by the flags and when the splits_eff CTAs of every
+// (request, kv head) form a supported cluster and all clusters fit at once.
+bool use_cluster_merge(const decode_attn_params* p, int32_t splits_eff) {
+  if ((p->flags & DA_FLAG_TWO_PASS) != 0 || splits_eff < 2 || p->batch < 1) return false;
+  return dattn::split_cluster_merge_fits(rows_of(p), splits_eff,
+                                         static_cast<int64_t>(p->batch) * p->num_kv_heads);
+}
 
 }  // namespace
 
@@ -256,7 +269,7 @@ int decode_attn_launch_count(const decode_attn_params* p, int32_t num_splits) {
   }
   rc = chunk_for_splits(p, num_splits, &chunk, &eff);
   if (rc != DA_OK) return rc;
-  return eff > 1 ? 2 : 1;
+  return eff > 1 && !use_cluster_merge(p, eff) ? 2 : 1;
 }
 
 }  // extern "C"
@@ -303,9 +316,11 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   }
   rc = chunk_for_splits(p, num_splits, &chunk, &eff);
   if (rc != DA_OK) return rc;
+  const bool cluster_merge = use_cluster_merge(p, eff);
   size_t need = 0;
   decode_attn_workspace_bytes(p, num_splits, &need);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+  if (!cluster_merge && need > 0 &&
+      (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
     return DA_ERR_WORKSPACE;
 
   CUtensorMap kmap, vmap;
@@ -330,8 +345,8 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   a.o_sh = p->o_stride_head;
   a.lse = lse;
   const size_t rows_total = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
-  a.part_o = eff > 1 ? static_cast<float*>(workspace) : nullptr;
-  a.part_lse = eff > 1 ? a.part_o + rows_total * eff * kHeadDim : nullptr;
+  a.part_o = eff > 1 && !cluster_merge ? static_cast<float*>(workspace) : nullptr;
+  a.part_lse = a.part_o != nullptr ? a.part_o + rows_total * eff * kHeadDim : nullptr;
   a.block_table = block_table;
   a.bt_stride = p->block_table_stride;
   a.seq_lens = seq_lens;
@@ -352,8 +367,8 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   a.scale_log2 = p->scale * 1.4426950408889634f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dattn::launch_split(kmap, vmap, a, st) != cudaSuccess) return DA_ERR_CUDA;
-  if (run_combine && eff > 1) {
+  if (dattn::launch_split(kmap, vmap, a, cluster_merge, st) != cudaSuccess) return DA_ERR_CUDA;
+  if (run_combine && eff > 1 && !cluster_merge) {
     dattn::CombineArgs c;
     c.part_o = a.part_o;
     c.part_lse = a.part_lse;
@@ -402,8 +417,9 @@ int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens, in
   if (p->batch == 0) return DA_OK;
   if (seq_lens == nullptr || out == nullptr || lse == nullptr) return DA_ERR_NULL_POINTER;
   if (num_splits < 1 || chunk_len < 1 || chunk_len % kTileTokens != 0 ||
-      ceil_div64(std::max(p->max_seq_len, 1), chunk_len) > num_splits)
+      ceil_div64(std::max(p->max_seq_len, 1), chunk_len) != num_splits)
     return DA_ERR_SPLITS;
+  if (use_cluster_merge(p, num_splits)) return DA_OK;  // the split pass already merged
   if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
       !stride_ok(p->o_stride_batch) || !stride_ok(p->o_stride_token) ||
       !stride_ok(p->o_stride_head))

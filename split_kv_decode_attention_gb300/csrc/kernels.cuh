@@ -43,9 +43,15 @@ struct CombineArgs {
   int max_seq_len, chunk_len, num_splits;
 };
 
-// Launch the split kernel over grid (num_splits, Hkv, B).
+// Launch the split kernel over grid (num_splits, Hkv, B).  With
+// cluster_merge the num_splits CTAs of each (kv head, request) run as one
+// thread-block cluster and write the final output (no partials, no combine).
 cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
-                         cudaStream_t stream);
+                         bool cluster_merge, cudaStream_t stream);
+
+// True when clusters of num_splits CTAs (2..16) are supported and the device
+// can hold num_clusters of them at once (one wave).
+bool split_cluster_merge_fits(int rows, int num_splits, int64_t num_clusters);
 
 // Resident split CTAs per SM for the kernel variant serving `rows` rows.
 int split_ctas_per_sm(int rows);

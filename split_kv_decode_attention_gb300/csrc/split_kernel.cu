@@ -41,6 +41,7 @@ namespace dattn {
 namespace {
 
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int NT, int STAGES, int TPS>
 struct SplitCfg {
@@ -53,8 +54,12 @@ struct SplitCfg {
   static constexpr int kRedStride = kHeadDim + 4;          // floats per row (bank spread)
   static constexpr int kRedBytes = TPS * kRows * kRedStride * 4;
   static_assert(kRedBytes <= kPipeBytes, "merge scratch must fit in the stage ring");
+  // cluster merge: this CTA's normalised output [kRows][128] fp32, after the
+  // warp-merge scratch in the (idle) stage ring, and its per-row LSE
+  static constexpr int kXoOffset = (kRedBytes + 127) / 128 * 128;
+  static_assert(kXoOffset + kRows * kHeadDim * 4 <= kPipeBytes, "cluster output must fit");
   static constexpr int kBarBytes = 2 * STAGES * 8;
-  static constexpr int kStatBytes = 2 * TPS * kRows * 4;
+  static constexpr int kStatBytes = 2 * TPS * kRows * 4 + kRows * 4;
   static constexpr int kSmemBytes = 1024 + kPipeBytes + kBarBytes + kStatBytes;
 };
 
@@ -69,7 +74,11 @@ __device__ __forceinline__ uint32_t load_u32(const uint16_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
 }
 
-template <int NT, int STAGES, int TPS>
+// CM (cluster merge): the num_splits CTAs of one (kv head, request) form one
+// thread-block cluster; instead of writing fp32 partials for the combine
+// kernel they merge their results through distributed shared memory and write
+// the final output themselves.
+template <int NT, int STAGES, int TPS, bool CM>
 __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
     split_kv_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const SplitArgs a) {
@@ -97,7 +106,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
     atomicOr(a.status, static_cast<int32_t>(bad));
   const int chunk = a.chunk_len;
   const int nsplit_b = L > 0 ? (L + chunk - 1) / chunk : 1;
-  if (split >= nsplit_b) return;
+  // (with the cluster merge every CTA stays: an empty chunk contributes 0 / -inf)
+  if (!CM && split >= nsplit_b) return;
   const int t_begin = split * chunk;
   const int t_end = min(L, t_begin + chunk);
   const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTileTokens - 1) / kTileTokens : 0;
@@ -110,6 +120,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
   uint64_t* empty_bar = full_bar + STAGES;
   float* stat_m = reinterpret_cast<float*>(empty_bar + STAGES);
   float* stat_l = stat_m + TPS * C::kRows;
+  float* xl = stat_l + TPS * C::kRows;  // cluster merge: this CTA's per-row LSE
 
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -184,6 +195,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
       // stages this warp issued
       for (int it = max(0, issued - STAGES); it < issued; ++it)
         mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1);
+    }
+    if constexpr (CM) {
+      // the consumers' two cluster barriers need every thread of the cluster
+      cluster_sync();
+      cluster_sync();
     }
     return;
   }
@@ -378,50 +394,124 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
     }
   named_barrier_sync(1, 32 * TPS);
 
-  const bool direct = nsplit_b == 1;
-  const int S = a.num_splits;
-  for (int idx = threadIdx.x; idx < a.rows * 32; idx += 32 * TPS) {
-    const int row = idx >> 5;
-    const int d = (idx & 31) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (CM) {
+    // ---- cluster merge: publish this CTA's (O, lse), then each CTA of the
+    // cluster reduces a slice of the rows over all CTAs through distributed
+    // shared memory (the same max / weighted-sum merge as the combine kernel)
+    float* xo = reinterpret_cast<float*>(smem + C::kXoOffset);
+    for (int idx = threadIdx.x; idx < a.rows * 32; idx += 32 * TPS) {
+      const int row = idx >> 5;
+      const int d = (idx & 31) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < TPS; ++w) {
-      const float4 x = *reinterpret_cast<const float4*>(red + (w * C::kRows + row) * C::kRedStride + d);
-      v.x += x.x;
-      v.y += x.y;
-      v.z += x.z;
-      v.w += x.w;
+      for (int w = 0; w < TPS; ++w) {
+        const float4 x =
+            *reinterpret_cast<const float4*>(red + (w * C::kRows + row) * C::kRedStride + d);
+        v.x += x.x;
+        v.y += x.y;
+        v.z += x.z;
+        v.w += x.w;
+      }
+      *reinterpret_cast<float4*>(xo + row * kHeadDim + d) = v;
     }
-    const int t = row / a.group;
-    const int h = kvh * a.group + (row - t * a.group);
-    if (direct) {
-      uint2 pk = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    if (threadIdx.x < a.rows) {
+      const int row = threadIdx.x;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < TPS; ++w) M = fmaxf(M, stat_m[w * C::kRows + row]);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float Ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < TPS; ++w)
+        Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
+      xl[row] = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -INFINITY;
+    }
+    cluster_sync();  // every CTA's (O, lse) is visible cluster-wide
+
+    const int S = gridDim.x;  // cluster = all chunks of this (kv head, request)
+    const uint32_t xo_addr = smem_addr(xo);
+    const uint32_t xl_addr = smem_addr(xl);
+    for (int u = split * 32 * TPS + threadIdx.x; u < a.rows * 32; u += S * 32 * TPS) {
+      const int row = u >> 5;
+      const int d = (u & 31) * 4;
+      float M = -INFINITY;
+      for (int r = 0; r < S; ++r)
+        M = fmaxf(M, ld_cluster_f32(map_to_rank(xl_addr + row * 4, r)));
+      float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float W = 0.f;
+      if (M != -INFINITY) {
+        for (int r = 0; r < S; ++r) {
+          const float w = ex2((ld_cluster_f32(map_to_rank(xl_addr + row * 4, r)) - M) * kLog2e);
+          const float4 x =
+              ld_cluster_f32x4(map_to_rank(xo_addr + (row * kHeadDim + d) * 4, r));
+          W += w;
+          acc4.x += w * x.x;
+          acc4.y += w * x.y;
+          acc4.z += w * x.z;
+          acc4.w += w * x.w;
+        }
+      }
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      const int t = row / a.group;
+      const int h = kvh * a.group + (row - t * a.group);
       *reinterpret_cast<uint2*>(a.out + static_cast<int64_t>(b) * a.o_sb +
                                 static_cast<int64_t>(t) * a.o_st +
-                                static_cast<int64_t>(h) * a.o_sh + d) = pk;
-    } else {
-      const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
-      *reinterpret_cast<float4*>(a.part_o + (prow * S + split) * kHeadDim + d) = v;
+                                static_cast<int64_t>(h) * a.o_sh + d) =
+          make_uint2(pack_bf16x2(acc4.x * inv, acc4.y * inv),
+                     pack_bf16x2(acc4.z * inv, acc4.w * inv));
+      if (d == 0) {
+        const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
+        a.lse[prow] = W > 0.f ? M + logf(W) : -INFINITY;
+      }
     }
-  }
-  if (threadIdx.x < a.rows) {
-    const int row = threadIdx.x;
-    float M = -INFINITY;
+    cluster_sync();  // no CTA leaves while another may still read its smem
+    return;
+  } else {
+  const bool direct = nsplit_b == 1;
+    const int S = a.num_splits;
+    for (int idx = threadIdx.x; idx < a.rows * 32; idx += 32 * TPS) {
+      const int row = idx >> 5;
+      const int d = (idx & 31) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < TPS; ++w) M = fmaxf(M, stat_m[w * C::kRows + row]);
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float Ls = 0.f;
+      for (int w = 0; w < TPS; ++w) {
+        const float4 x = *reinterpret_cast<const float4*>(red + (w * C::kRows + row) * C::kRedStride + d);
+        v.x += x.x;
+        v.y += x.y;
+        v.z += x.z;
+        v.w += x.w;
+      }
+      const int t = row / a.group;
+      const int h = kvh * a.group + (row - t * a.group);
+      if (direct) {
+        uint2 pk = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+        *reinterpret_cast<uint2*>(a.out + static_cast<int64_t>(b) * a.o_sb +
+                                  static_cast<int64_t>(t) * a.o_st +
+                                  static_cast<int64_t>(h) * a.o_sh + d) = pk;
+      } else {
+        const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
+        *reinterpret_cast<float4*>(a.part_o + (prow * S + split) * kHeadDim + d) = v;
+      }
+    }
+    if (threadIdx.x < a.rows) {
+      const int row = threadIdx.x;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < TPS; ++w)
-      Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
-    const float lse = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -INFINITY;
-    const int t = row / a.group;
-    const int h = kvh * a.group + (row - t * a.group);
-    const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
-    if (direct)
-      a.lse[prow] = lse;
-    else
-      a.part_lse[prow * S + split] = lse;
+      for (int w = 0; w < TPS; ++w) M = fmaxf(M, stat_m[w * C::kRows + row]);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float Ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < TPS; ++w)
+        Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
+      const float lse = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -INFINITY;
+      const int t = row / a.group;
+      const int h = kvh * a.group + (row - t * a.group);
+      const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
+      if (direct)
+        a.lse[prow] = lse;
+      else
+        a.part_lse[prow * S + split] = lse;
+    }
   }
 }
 
@@ -439,68 +529,140 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
 constexpr int kStages = DATTN_STAGES;
 constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
 
-template <int NT>
+template <int NT, bool CM>
 struct Variant {
   using C = SplitCfg<NT, kStages, kTilesPerStage>;
-  static constexpr auto kernel = split_kv_kernel<NT, kStages, kTilesPerStage>;
+  static constexpr auto kernel = split_kv_kernel<NT, kStages, kTilesPerStage, CM>;
 };
 
+constexpr int kMaxDev = 64;
+constexpr int kMaxCluster = 16;  // non-portable cluster size limit
 std::mutex g_attr_mu;
-bool g_attr_done[2][64];
+bool g_attr_done[2][2][kMaxDev];
+// cached cudaOccupancyMaxActiveClusters per (NT, cluster size, device); -1 unknown
+int g_max_clusters[2][kMaxCluster + 1][kMaxDev];
+bool g_max_clusters_init = false;
 
-template <int NT>
-cudaError_t ensure_attrs() {
+template <int NT, bool CM>
+cudaError_t ensure_attrs(int* dev_out = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  if (dev_out) *dev_out = dev;
   std::lock_guard<std::mutex> lk(g_attr_mu);
-  if (!g_attr_done[NT - 1][dev]) {
-    e = cudaFuncSetAttribute(Variant<NT>::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Variant<NT>::C::kSmemBytes);
+  if (!g_attr_done[NT - 1][CM][dev]) {
+    e = cudaFuncSetAttribute(Variant<NT, CM>::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Variant<NT, CM>::C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    g_attr_done[NT - 1][dev] = true;
+    if (CM) {
+      e = cudaFuncSetAttribute(Variant<NT, CM>::kernel,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    g_attr_done[NT - 1][CM][dev] = true;
   }
   return cudaSuccess;
 }
 
-template <int NT>
-cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitArgs& a,
-                      cudaStream_t st) {
-  cudaError_t e = ensure_attrs<NT>();
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
+template <int NT, bool CM>
+void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const SplitArgs& a,
+                 cudaStream_t st) {
+  cfg = {};
   cfg.gridDim = dim3(a.num_splits, a.num_kv_heads, a.batch);
-  cfg.blockDim = dim3(Variant<NT>::C::kThreads);
-  cfg.dynamicSmemBytes = Variant<NT>::C::kSmemBytes;
+  cfg.blockDim = dim3(Variant<NT, CM>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT, CM>::C::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, Variant<NT>::kernel, km, vm, a);
+  if (CM) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(a.num_splits);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+}
+
+template <int NT, bool CM>
+cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitArgs& a,
+                      cudaStream_t st) {
+  cudaError_t e = ensure_attrs<NT, CM>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  fill_config<NT, CM>(cfg, attr, a, st);
+  return cudaLaunchKernelEx(&cfg, Variant<NT, CM>::kernel, km, vm, a);
 }
 
 template <int NT>
 int ctas_per_sm_nt() {
-  if (ensure_attrs<NT>() != cudaSuccess) return 1;
+  if (ensure_attrs<NT, false>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Variant<NT>::kernel, Variant<NT>::C::kThreads,
-                                                    Variant<NT>::C::kSmemBytes) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Variant<NT, false>::kernel,
+                                                    Variant<NT, false>::C::kThreads,
+                                                    Variant<NT, false>::C::kSmemBytes) !=
+          cudaSuccess ||
       n < 1)
     return 1;
+  return n;
+}
+
+// How many clusters of `splits` CTAs the device can hold at once.
+template <int NT>
+int max_active_clusters(int splits) {
+  int dev = 0;
+  if (ensure_attrs<NT, true>(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (!g_max_clusters_init) {
+      for (auto& x : g_max_clusters)
+        for (auto& y : x)
+          for (int& z : y) z = -1;
+      g_max_clusters_init = true;
+    }
+    if (g_max_clusters[NT - 1][splits][dev] >= 0) return g_max_clusters[NT - 1][splits][dev];
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(splits), 1, 1);
+  cfg.blockDim = dim3(Variant<NT, true>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT, true>::C::kSmemBytes;
+  cudaLaunchAttribute cl[1];
+  cl[0].id = cudaLaunchAttributeClusterDimension;
+  cl[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  cl[0].val.clusterDim.y = 1;
+  cl[0].val.clusterDim.z = 1;
+  cfg.attrs = cl;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, Variant<NT, true>::kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear the (non-sticky) error of a rejected query
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  g_max_clusters[NT - 1][splits][dev] = n;
   return n;
 }
 
 }  // namespace
 
 cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
-                         cudaStream_t stream) {
-  if (a.rows <= 8) return launch_nt<1>(k_map, v_map, a, stream);
-  return launch_nt<2>(k_map, v_map, a, stream);
+                         bool cluster_merge, cudaStream_t stream) {
+  if (a.rows <= 8)
+    return cluster_merge ? launch_nt<1, true>(k_map, v_map, a, stream)
+                         : launch_nt<1, false>(k_map, v_map, a, stream);
+  return cluster_merge ? launch_nt<2, true>(k_map, v_map, a, stream)
+                       : launch_nt<2, false>(k_map, v_map, a, stream);
 }
 
 int split_ctas_per_sm(int rows) { return rows <= 8 ? ctas_per_sm_nt<1>() : ctas_per_sm_nt<2>(); }
+
+bool split_cluster_merge_fits(int rows, int num_splits, int64_t num_clusters) {
+  if (num_splits < 2 || num_splits > kMaxCluster || num_clusters < 1) return false;
+  const int n = rows <= 8 ? max_active_clusters<1>(num_splits) : max_active_clusters<2>(num_splits);
+  return n >= num_clusters;
+}
 
 }  // namespace dattn

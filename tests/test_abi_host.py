@@ -65,7 +65,7 @@ def _call(lib, p, **kw):
 
 @pytest.mark.parametrize("field,value,code", [
     ("head_dim", 64, -3), ("num_kv_heads", 3, -2), ("q_len", 0, -2), ("batch", -1, -2),
-    ("max_seq_len", -5, -2), ("reserved0", 1, -2)])
+    ("max_seq_len", -5, -2), ("flags", 2, -2)])
 def test_shape_errors_are_reported_before_launch(lib, field, value, code):
     p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 0, 0, 0, 64, False)
     setattr(p, field, value)

@@ -76,7 +76,8 @@ def test_split_partials_match_oracle_on_each_chunk(binding):
                         hi=900, causal=True, seed=42)
     inp = W.make_host_inputs(shp)
     q, k, v, bt, lens = to_device(inp)
-    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True)
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True,
+                                    two_pass=True)       # partials are only kept in two passes
     S = 4
     chunk = binding.decode_attn_chunk_len(p, S)
     ws = torch.full(((binding.decode_attn_workspace_bytes(p, S) + 3) // 4,), float("nan"),
@@ -103,6 +104,7 @@ def test_combine_alone_matches_oracle_merge(binding):
     B, T, Hq, S, chunk = 3, 2, 4, 6, 64
     lens = np.array([S * chunk, 2 * chunk - 5, chunk], np.int32)   # 6, 2 and 1 chunks
     p = binding.decode_attn_params_init(B, T, Hq, 1, 128, 0, 0, 0, S * chunk, False)
+    p.flags = binding.DA_FLAG_TWO_PASS       # the workspace holds partials to merge
     part_o = rng.standard_normal((B, T, Hq, S, 128)).astype(np.float32)
     part_l = (rng.standard_normal((B, T, Hq, S)) * 5).astype(np.float32)
     part_l[0, 0, 0, 2] = -np.inf
@@ -179,7 +181,7 @@ def test_workspace_too_small_is_rejected(binding):
     shp = W.small_shape("ws", batch=2, num_q_heads=4, num_kv_heads=1, lo=500, hi=500,
                         paged=False, seed=47)
     q, k, v, _, lens = to_device(W.make_host_inputs(shp))
-    p = binding.params_from_tensors(q, k, None, max_seq_len=500)
+    p = binding.params_from_tensors(q, k, None, max_seq_len=500, two_pass=True)
     need = binding.decode_attn_workspace_bytes(p, 4)
     ws = torch.empty(need // 4 - 1, dtype=torch.float32, device="cuda")
     out = torch.empty_like(q)

@@ -36,9 +36,9 @@ def run(binding, inp, num_splits=0, status=None, **kw):
     return out, lse
 
 
-def check(binding, inp, num_splits=0):
+def check(binding, inp, num_splits=0, two_pass=False):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out, lse = run(binding, inp, num_splits, status=status)
+    out, lse = run(binding, inp, num_splits, status=status, two_pass=two_pass)
     ref_o, ref_l = oracle.decode_attention_inputs(inp)
     assert int(status.item()) == 0
     assert_out_close(bf16_tensor_to_f64(out), ref_o)
@@ -61,15 +61,16 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("two_pass", [False, True], ids=["merge-auto", "two-pass"])
 @pytest.mark.parametrize("splits", [1, 2, 7, 0])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_small_workloads_match_oracle(binding, case, splits):
+def test_small_workloads_match_oracle(binding, case, splits, two_pass):
     name, G, T, causal, paged, ps, lo, hi = case
     shp = W.small_shape(name, batch=4, q_len=T, num_q_heads=2 * G, num_kv_heads=2,
                         lo=lo, hi=hi, paged=paged, page_size=ps, causal=causal,
                         peaked=0.05 if "peaked" in name else 0.0, seed=100 + G + T)
     inp = W.make_host_inputs(shp)
-    check(binding, inp, splits)
+    check(binding, inp, splits, two_pass)
 
 
 @pytest.mark.parametrize("splits", [1, 3])
@@ -101,5 +102,27 @@ def test_long_single_request_many_splits(binding):
     shp = W.small_shape("long", batch=1, num_q_heads=4, num_kv_heads=1, lo=20011,
                         hi=20011, paged=False, seed=33)
     inp = W.make_host_inputs(shp)
-    for s in (1, 5, 40, 0):
+    for s in (1, 5, 16, 40, 0):
         check(binding, inp, s)
+        check(binding, inp, s, two_pass=True)
+
+
+def test_cluster_merge_is_one_launch_and_matches_two_pass(binding):
+    """2..16 chunks per head that fit at once merge through a thread-block
+    cluster (one launch); more chunks, or the two-pass flag, use partials and
+    the combine kernel.  Both forms agree with the oracle."""
+    shp = W.small_shape("cm", batch=3, q_len=2, num_q_heads=16, num_kv_heads=4, lo=100,
+                        hi=4000, paged=True, causal=True, seed=34)
+    inp = W.make_host_inputs(shp)
+    q, k, v, bt, lens = to_device(inp)
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True)
+    p2 = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True,
+                                     two_pass=True)
+    for S in (2, 9, 16):
+        assert binding.decode_attn_launch_count(p, S) == 1
+        assert binding.decode_attn_launch_count(p2, S) == 2
+        o1, l1 = check(binding, inp, S)
+        o2, l2 = check(binding, inp, S, two_pass=True)
+        assert_out_close(bf16_tensor_to_f64(o1), bf16_tensor_to_f64(o2), what="cluster vs two-pass")
+    # beyond the largest cluster (after rounding the chunk length to 16 tokens)
+    assert binding.decode_attn_launch_count(p, 40) == 2
