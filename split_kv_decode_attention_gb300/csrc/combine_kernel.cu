@@ -42,17 +42,25 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const Comb
   const int S = a.num_splits;
   const float* pl = a.part_lse + row * S;
   const float* po = a.part_o + row * S * kHeadDim + lane * 4;
-  // lane i holds lse of splits i, i + 32, ...; the row max by warp shuffles
+  uint16_t* orow = a.out + static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(t) * a.o_st +
+                   static_cast<int64_t>(h) * a.o_sh + lane * 4;
+
+  // splits in groups of 32: lane j holds lse of split s0 + j; the group's
+  // partial rows are loaded kBatch at a time, the first batch in the same
+  // round trip as the LSEs (the loads do not depend on the weights)
+  constexpr int kBatch = 8;
   float M = -INFINITY;
   for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
+  float4 v[kBatch];
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j)
+    v[j] = j < n ? *reinterpret_cast<const float4*>(po + static_cast<int64_t>(j) * kHeadDim)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 16));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 8));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 4));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
-
-  uint16_t* orow = a.out + static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(t) * a.o_st +
-                   static_cast<int64_t>(h) * a.o_sh + lane * 4;
   if (M == -INFINITY) {
     *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
     if (lane == 0) a.lse[row] = -INFINITY;
@@ -60,19 +68,17 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const Comb
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float W = 0.f;
-  // splits in groups of 32: lane j owns the weight of split s0 + j; each lane
-  // then streams the group's partial rows, kBatch loads in flight at a time
-  constexpr int kBatch = 8;
   for (int s0 = 0; s0 < n; s0 += 32) {
     const int cnt = min(32, n - s0);
     const float w_mine = lane < cnt ? ex2((pl[s0 + lane] - M) * kLog2e) : 0.f;
     for (int j0 = 0; j0 < cnt; j0 += kBatch) {
-      float4 v[kBatch];
+      if (s0 + j0 > 0) {  // batch 0 of group 0 is already in flight
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j)
-        v[j] = j0 + j < cnt ? *reinterpret_cast<const float4*>(
-                                  po + static_cast<int64_t>(s0 + j0 + j) * kHeadDim)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < kBatch; ++j)
+          v[j] = j0 + j < cnt ? *reinterpret_cast<const float4*>(
+                                    po + static_cast<int64_t>(s0 + j0 + j) * kHeadDim)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const float w = __shfl_sync(kFull, w_mine, (j0 + j) & 31);

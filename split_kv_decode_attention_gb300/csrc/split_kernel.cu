@@ -662,6 +662,8 @@ int split_ctas_per_sm(int rows) { return rows <= 8 ? ctas_per_sm_nt<1>() : ctas_
 bool split_cluster_merge_fits(int rows, int num_splits, int64_t num_clusters) {
   if (num_splits < 2 || num_splits > kMaxCluster || num_clusters < 1) return false;
   const int n = rows <= 8 ? max_active_clusters<1>(num_splits) : max_active_clusters<2>(num_splits);
+  // all clusters resident at once: in multi-wave grids the idle CTAs of short
+  // requests hold slots (GB300 sweeps: 1.5-2x slower than partials + combine)
   return n >= num_clusters;
 }
 
