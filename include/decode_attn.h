@@ -65,7 +65,8 @@ extern "C" {
 #endif
 
 #define DECODE_ATTN_HEAD_DIM 128   /* the only supported head_dim */
-#define DECODE_ATTN_MAX_ROWS 16    /* (Hq / Hkv) * q_len must not exceed this */
+#define DECODE_ATTN_MAX_ROWS 128   /* (Hq / Hkv) * q_len must not exceed this;
+                                      above 16 rows the tcgen05 kernel runs */
 #define DECODE_ATTN_TOKEN_TILE 16  /* chunk_len and page_size are multiples */
 
 /* return codes */

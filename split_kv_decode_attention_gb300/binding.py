@@ -16,7 +16,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libdecode_attn.so")
 
 HEAD_DIM = 128
-MAX_ROWS = 16
+MAX_ROWS = 128
 TOKEN_TILE = 16
 
 DA_OK = 0

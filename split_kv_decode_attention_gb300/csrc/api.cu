@@ -455,7 +455,7 @@ const char* decode_attn_status_string(int code) {
     case DA_ERR_BAD_SHAPE: return "invalid sizes (batch, heads, q_len, lengths or paging)";
     case DA_ERR_HEAD_DIM: return "head_dim must be 128";
     case DA_ERR_PAGE_SIZE: return "page_size must be a positive multiple of 16";
-    case DA_ERR_ROWS: return "(num_q_heads / num_kv_heads) * q_len exceeds 16";
+    case DA_ERR_ROWS: return "(num_q_heads / num_kv_heads) * q_len exceeds 128";
     case DA_ERR_ALIGNMENT: return "pointer or stride misaligned (16-byte bases, strides multiple of 8 elements)";
     case DA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case DA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";

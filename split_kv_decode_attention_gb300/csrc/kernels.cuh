@@ -6,11 +6,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "decode_attn.h"
+
 namespace dattn {
 
 constexpr int kHeadDim = 128;
 constexpr int kTileTokens = 16;        // tokens per TMA box / per MMA tile
-constexpr int kMaxRows = 16;           // GQA group x q_len rows per CTA
+constexpr int kMaxRows = 128;          // GQA group x q_len rows per CTA
+constexpr int kMaxNarrowRows = 16;     // above this: the tcgen05 kernel
 
 // Arguments of the split kernel (one CTA per (chunk, kv head, request)).
 struct SplitArgs {
@@ -43,6 +46,42 @@ struct CombineArgs {
   int max_seq_len, chunk_len, num_splits;
 };
 
+// Physical page ids of a chunk's 16-token tiles, for the TMA producer warp.
+// Lane i holds the id of tile base + i of the current 32-tile window and of
+// the next window, loaded a full window (32 tiles) before it is needed, so
+// the block-table latency never sits in front of a TMA issue.  Out-of-range
+// entries read as page 0 and set DA_STATUS_BAD_PAGE.  All lanes of the warp
+// must call get() together with the same tile.
+struct PageWindow {
+  const int32_t* bt_row;  // this request's block-table row (nullptr: contiguous)
+  int t_begin, n_tiles, page_size, num_pages, lane;
+  int32_t* status;
+  int cur, nxt, base;
+
+  __device__ __forceinline__ int load(int tile) const {
+    if (bt_row == nullptr || tile >= n_tiles) return 0;
+    int pg = __ldg(bt_row + (t_begin + tile * 16) / page_size);
+    if (pg < 0 || pg >= num_pages) {
+      if (status != nullptr) atomicOr(status, static_cast<int32_t>(DA_STATUS_BAD_PAGE));
+      pg = 0;
+    }
+    return pg;
+  }
+  __device__ __forceinline__ void init() {
+    base = 0;
+    cur = load(lane);
+    nxt = load(32 + lane);
+  }
+  __device__ __forceinline__ int get(int tile) {
+    while (tile >= base + 32) {
+      cur = nxt;
+      base += 32;
+      nxt = load(base + 32 + lane);
+    }
+    return __shfl_sync(0xffffffffu, cur, tile - base);
+  }
+};
+
 // Launch the split kernel over grid (num_splits, Hkv, B).  With
 // cluster_merge the num_splits CTAs of each (kv head, request) run as one
 // thread-block cluster and write the final output (no partials, no combine).
@@ -55,6 +94,12 @@ bool split_cluster_merge_fits(int rows, int num_splits, int64_t num_clusters);
 
 // Resident split CTAs per SM for the kernel variant serving `rows` rows.
 int split_ctas_per_sm(int rows);
+
+// Launch the tcgen05 kernel for 17..128 rows per kv head (same grid, same
+// outputs and partials as launch_split without cluster merge).
+cudaError_t launch_wide(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
+                        cudaStream_t stream);
+int wide_ctas_per_sm();
 
 // Launch the combine kernel (one warp per output row).
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);

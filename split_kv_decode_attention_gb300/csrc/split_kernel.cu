@@ -54,6 +54,7 @@ struct SplitCfg {
   static constexpr int kRedStride = kHeadDim + 4;          // floats per row (bank spread)
   static constexpr int kRedBytes = TPS * kRows * kRedStride * 4;
   static_assert(kRedBytes <= kPipeBytes, "merge scratch must fit in the stage ring");
+  static_assert(4 * TPS <= 32, "one TMA box per producer lane");
   // cluster merge: this CTA's normalised output [kRows][128] fp32, after the
   // warp-merge scratch in the (idle) stage ring, and its per-row LSE
   static constexpr int kXoOffset = (kRedBytes + 127) / 128 * 128;
@@ -141,23 +142,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
     const uint64_t policy = l2_evict_first_policy();
     const int32_t* bt_row = a.paged ? a.block_table + static_cast<int64_t>(b) * a.bt_stride : nullptr;
     // physical page of tile (it * TPS + lane); fetched one stage ahead
-    auto page_of = [&](int it) -> int {
-      const int tile = it * TPS + lane;
-      if (!a.paged || lane >= TPS || tile >= n_tiles) return 0;
-      const int tok = t_begin + tile * kTileTokens;
-      int pg = __ldg(bt_row + tok / a.page_size);
-      if (pg < 0 || pg >= a.num_pages) {
-        if (a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_BAD_PAGE));
-        pg = 0;
-      }
-      return pg;
-    };
-    int pg_next = n_iters > 0 ? page_of(0) : 0;
+    PageWindow pw{bt_row, t_begin, n_tiles, a.page_size, a.num_pages, lane, a.status, 0, 0, 0};
+    if (a.paged) pw.init();
     int issued = 0;
     bool ok = true;
     for (int it = 0; it < n_iters; ++it) {
-      const int pg_cur = pg_next;
-      if (it + 1 < n_iters) pg_next = page_of(it + 1);
       const int s = it % STAGES;
       const int use = it / STAGES;
       int good = 1;
@@ -168,23 +157,27 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
         break;
       }
       const int tiles_here = min(TPS, n_tiles - it * TPS);
-      int pgs[TPS];
+      // page id of the tile this lane loads (lane / 4), picked in registers
+      int my_pg = 0;
 #pragma unroll
-      for (int i = 0; i < TPS; ++i) pgs[i] = __shfl_sync(kFull, pg_cur, i);
-      if (lane == 0) {
+      for (int i = 0; i < TPS; ++i) {
+        const int pg = a.paged ? pw.get(it * TPS + i) : 0;
+        if ((lane >> 2) == i) my_pg = pg;
+      }
+      if (lane == 0)
         mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(tiles_here * 2 * C::kTileBytes));
-        uint8_t* stage = smem + s * C::kStageBytes;
-        for (int i = 0; i < tiles_here; ++i) {
-          const int tok = t_begin + (it * TPS + i) * kTileTokens;
-          const int grp = a.paged ? pgs[i] : b;
-          const int tin = a.paged ? tok % a.page_size : tok;
-          uint8_t* kd = stage + i * C::kTileBytes;
-          uint8_t* vd = stage + (TPS + i) * C::kTileBytes;
-          tma_load_4d(kd, &k_map, &full_bar[s], 0, kvh, tin, grp, policy);
-          tma_load_4d(kd + C::kHalfBytes, &k_map, &full_bar[s], 64, kvh, tin, grp, policy);
-          tma_load_4d(vd, &v_map, &full_bar[s], 0, kvh, tin, grp, policy);
-          tma_load_4d(vd + C::kHalfBytes, &v_map, &full_bar[s], 64, kvh, tin, grp, policy);
-        }
+      __syncwarp();
+      // one TMA box per lane (tile = lane / 4; K or V, d-half from lane % 4)
+      if (lane < tiles_here * 4) {
+        const int i = lane >> 2;
+        const int tok = t_begin + (it * TPS + i) * kTileTokens;
+        const int grp = a.paged ? my_pg : b;
+        const int tin = a.paged ? tok % a.page_size : tok;
+        const int half = lane & 1;
+        const bool is_v = (lane & 2) != 0;
+        uint8_t* dst = smem + s * C::kStageBytes + ((is_v ? TPS : 0) + i) * C::kTileBytes +
+                       half * C::kHalfBytes;
+        tma_load_4d(dst, is_v ? &v_map : &k_map, &full_bar[s], half * 64, kvh, tin, grp, policy);
       }
       ++issued;
       __syncwarp();
@@ -650,6 +643,7 @@ int max_active_clusters(int splits) {
 
 cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
                          bool cluster_merge, cudaStream_t stream) {
+  if (a.rows > kMaxNarrowRows) return launch_wide(k_map, v_map, a, stream);
   if (a.rows <= 8)
     return cluster_merge ? launch_nt<1, true>(k_map, v_map, a, stream)
                          : launch_nt<1, false>(k_map, v_map, a, stream);
@@ -657,10 +651,14 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
                        : launch_nt<2, false>(k_map, v_map, a, stream);
 }
 
-int split_ctas_per_sm(int rows) { return rows <= 8 ? ctas_per_sm_nt<1>() : ctas_per_sm_nt<2>(); }
+int split_ctas_per_sm(int rows) {
+  if (rows > kMaxNarrowRows) return wide_ctas_per_sm();
+  return rows <= 8 ? ctas_per_sm_nt<1>() : ctas_per_sm_nt<2>();
+}
 
 bool split_cluster_merge_fits(int rows, int num_splits, int64_t num_clusters) {
-  if (num_splits < 2 || num_splits > kMaxCluster || num_clusters < 1) return false;
+  if (num_splits < 2 || num_splits > kMaxCluster || num_clusters < 1 || rows > kMaxNarrowRows)
+    return false;
   const int n = rows <= 8 ? max_active_clusters<1>(num_splits) : max_active_clusters<2>(num_splits);
   // all clusters resident at once: in multi-wave grids the idle CTAs of short
   // requests hold slots (GB300 sweeps: 1.5-2x slower than partials + combine)

@@ -107,6 +107,20 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# Wider speculative verify (G x q_len = 64 and 128 query rows per KV head):
+# the same synthetic recipe as c5, with 8 and 16 draft tokens.
+WIDE_WORKLOADS = {
+    "w64_b32_q8_h64kv8_causal_L1024-16384_paged": DecodeShape(
+        "w64_b32_q8_h64kv8_causal_L1024-16384_paged", batch=32, q_len=8,
+        num_q_heads=64, num_kv_heads=8, seq_len_lo=1024, seq_len_hi=16384,
+        paged=True, causal=True, seed=1006),
+    "w128_b16_q16_h64kv8_causal_L1024-16384_paged": DecodeShape(
+        "w128_b16_q16_h64kv8_causal_L1024-16384_paged", batch=16, q_len=16,
+        num_q_heads=64, num_kv_heads=8, seq_len_lo=1024, seq_len_hi=16384,
+        paged=True, causal=True, seed=1007),
+}
+WORKLOADS.update(WIDE_WORKLOADS)
+
 
 @dataclasses.dataclass
 class DecodeInputs:

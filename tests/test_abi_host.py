@@ -73,7 +73,9 @@ def test_shape_errors_are_reported_before_launch(lib, field, value, code):
 
 
 def test_too_many_rows_rejected(lib):
-    p = binding.decode_attn_params_init(1, 4, 32, 4, 128, 0, 0, 0, 64, True)  # 8 x 4 = 32 rows
+    p = binding.decode_attn_params_init(1, 4, 64, 2, 128, 0, 0, 0, 64, True)  # 32 x 4 = 128 rows
+    assert _call(lib, p) != -5
+    p = binding.decode_attn_params_init(1, 5, 64, 2, 128, 0, 0, 0, 64, True)  # 32 x 5 = 160 rows
     assert _call(lib, p) == -5
 
 

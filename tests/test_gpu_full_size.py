@@ -32,7 +32,7 @@ def host_bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("name", W.WORKLOAD_ORDER)
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER + list(W.WIDE_WORKLOADS))
 def test_full_size_workload_sampled_rows_match_oracle(binding, name):
     shape = W.WORKLOADS[name]
     inp = W.make_device_inputs(shape, device="cuda")

@@ -58,6 +58,13 @@ CASES = [
     ("mha_q16_causal", 1, 16, True, True, 16, 16, 300),
     ("gqa4_q2_page32", 4, 2, True, True, 32, 2, 700),
     ("gqa8_page64", 8, 1, False, True, 64, 1, 500),
+    # wide query groups (17..128 rows per kv head): the tcgen05 kernel
+    ("wide20_gqa4_q5_causal_contig", 4, 5, True, False, 16, 5, 600),
+    ("wide32_gqa8_q4_causal", 8, 4, True, True, 16, 4, 900),
+    ("wide64_gqa8_q8_causal", 8, 8, True, True, 16, 8, 700),
+    ("wide64_gqa16_q4_nocausal_page32", 16, 4, False, True, 32, 4, 500),
+    ("wide128_gqa16_q8_causal", 16, 8, True, True, 16, 8, 400),
+    ("wide128_mha_q128_causal", 1, 128, True, True, 16, 128, 400),
 ]
 
 
@@ -83,6 +90,40 @@ def test_edge_lengths_including_empty_requests(binding, splits):
     o = bf16_tensor_to_f64(out)
     assert np.all(o[0] == 0) and np.all(o[10] == 0)
     assert np.all(np.isneginf(lse.cpu().numpy()[[0, 10]]))
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_wide_edge_lengths_including_empty_requests(binding, splits):
+    lens = np.array([0, 4, 15, 16, 17, 63, 64, 65, 127, 129, 0, 250], np.int32)
+    shp = W.small_shape("wide_edges", batch=len(lens), q_len=4, num_q_heads=16,
+                        num_kv_heads=2, lo=0, hi=256, paged=True, causal=True, seed=35)
+    inp = W.make_host_inputs(shp, seq_lens=lens)
+    out, lse = check(binding, inp, splits)
+    assert np.all(bf16_tensor_to_f64(out)[[0, 10]] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[[0, 10]]))
+
+
+@pytest.mark.parametrize("direction", [1.0, -1.0])
+def test_wide_running_max_keeps_moving(binding, direction):
+    """Scores that drift steadily up (or down) along the sequence make the
+    running max grow by more than 2^8 many times within one chunk, so the
+    tcgen05 kernel's lazy O rescaling runs repeatedly."""
+    rng = np.random.default_rng(36)
+    B, T, Hq, Hkv, L = 2, 8, 64, 4, 1500
+    q = rng.standard_normal((B, T, Hq, 128)).astype(np.float32)
+    k = rng.standard_normal((B, L, Hkv, 128)).astype(np.float32) * 0.3
+    # add a component along the mean query direction that grows with j
+    qdir = q.reshape(B, T, Hkv, Hq // Hkv, 128).mean(axis=(1, 3))          # [B, Hkv, 128]
+    qdir /= np.linalg.norm(qdir, axis=-1, keepdims=True)
+    ramp = direction * np.linspace(0, 60, L, dtype=np.float32)              # scale x ramp >> 2^8
+    k += ramp[None, :, None, None] * qdir[:, None, :, :]
+    v = rng.standard_normal((B, L, Hkv, 128)).astype(np.float32)
+    inp = W.DecodeInputs(W.small_shape("ramp", batch=B, q_len=T, num_q_heads=Hq,
+                                       num_kv_heads=Hkv, lo=L, hi=L, paged=False, causal=True),
+                         W.f32_to_bf16_bits(q), W.f32_to_bf16_bits(k), W.f32_to_bf16_bits(v),
+                         None, np.full(B, L, np.int32), L, 0, 0)
+    for S in (1, 2):
+        check(binding, inp, S)
 
 
 def test_all_requests_empty(binding):
