@@ -6,7 +6,7 @@ inputs.  Prints ONE JSON line (rank 0):
 
   value        KV-read GB/s = algorithmic K+V bytes / device time per call
   ms_per_step  device time per call (CUDA events on the launching stream)
-  roofline     the split kernel's achieved GB/s against the measured HBM peak
+  roofline     the K/V-reading kernel's achieved GB/s against the measured HBM peak
   e2e          the same metric through the public call with per-step
                host->device inputs (q, seq_lens, block table) and
                device->host outputs (out, lse)
@@ -44,7 +44,19 @@ DEFAULT_WORKLOAD = "c2_b1_mha32_L131072"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["split_kernel.cu", "ptx.cuh", "kernels.cuh"]
+# the kernel that reads K/V, by rows per KV head (q_len x heads per KV head),
+# and the sources its machine code depends on (a committed ncu summary is
+# trusted only while their hash matches)
+KERNEL_SOURCES = {
+    "split_kv_kernel": ["split_kernel.cu", "ptx.cuh", "kernels.cuh"],
+    "wide_kernel": ["wide_kernel.cu", "tcgen05.cuh", "ptx.cuh", "kernels.cuh"],
+}
+NARROW_MAX_ROWS = 16
+
+
+def dominant_kernel(shape) -> str:
+    rows = shape.q_len * (shape.num_q_heads // shape.num_kv_heads)
+    return "split_kv_kernel" if rows <= NARROW_MAX_ROWS else "wide_kernel"
 
 
 def parse_args(argv=None):
@@ -74,25 +86,25 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "split_kv_kernel") -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "split_kv_decode_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per split-kernel launch from the committed ncu summary, or
+def profiled_traffic(workload: str, kernel: str = "split_kv_kernel"):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
     None when there is none or the kernel sources changed since it was taken."""
-    path = os.path.join(PROFILE_DIR, f"split_kv_kernel_{workload}.md")
+    path = os.path.join(PROFILE_DIR, f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m_b or not m_h or m_h.group(1) != kernel_source_hash():
+    if not m_b or not m_h or m_h.group(1) != kernel_source_hash(kernel):
         return None
     return int(m_b.group(1))
 
@@ -340,7 +352,8 @@ def run_ours(args, dist: "Dist"):
     peak, peak_kind = load_peaks()
     split_mean_ms = float(split_ms.mean())
     achieved = nbytes["total"] / (split_mean_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload)
+    kernel = dominant_kernel(shape)
+    traffic = profiled_traffic(args.workload, kernel)
 
     # informational, outside the timed steps: the same call as one
     # decode_attn() with no event between the two launches, so the combine
@@ -389,7 +402,7 @@ def run_ours(args, dist: "Dist"):
                          f"inputs larger than L2 ({kv_resident / 2**30:.2f} GiB resident K/V)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "split_kv_kernel", "peak_kind": f"{peak_kind} (copy, burst)",
+                     "kernel": kernel, "peak_kind": f"{peak_kind} (copy, burst)",
                      "algorithmic_bytes_per_launch": nbytes["total"],
                      "split_us": round(split_mean_ms * 1e3, 2),
                      "combine_us": round(float(comb_ms.mean()) * 1e3, 2)},

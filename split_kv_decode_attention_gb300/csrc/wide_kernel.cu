@@ -32,6 +32,7 @@
 #include "decode_attn.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace dattn {
 namespace {
