@@ -42,36 +42,41 @@ constexpr int kWRows = 128;                  // MMA M: query rows per CTA (padde
 constexpr int kWTok = 64;                    // keys per stage (MMA N of S)
 constexpr int kWTiles = kWTok / kTileTokens; // 16-token page tiles per stage
 #ifndef DATTN_WIDE_STAGES
-#define DATTN_WIDE_STAGES 4
+#define DATTN_WIDE_STAGES 6
 #endif
 constexpr int kWStages = DATTN_WIDE_STAGES;  // K/V stages in flight
-constexpr int kWThreads = 320;               // warps 0-7 softmax (2 groups), 8 TMA, 9 MMA
-constexpr int kWProducerWarp = 8;
-constexpr int kWMmaWarp = 9;
+#ifndef DATTN_WIDE_PRODUCERS
+#define DATTN_WIDE_PRODUCERS 4
+#endif
+// TMA copies issued by one warp are serialised (~130 cycles per box), so
+// several producer warps share each stage's boxes.
+constexpr int kWProducers = DATTN_WIDE_PRODUCERS;
+constexpr int kWProducerWarp = 8;            // warps 0-7 softmax (2 groups), then TMA, then MMA
+constexpr int kWMmaWarp = kWProducerWarp + kWProducers;
+constexpr int kWThreads = 32 * (kWMmaWarp + 1);
+constexpr int kWBoxes = 4 * kWTiles;         // per stage: tiles x {K, V} x 2 d-halves, 2 KB each
+constexpr int kWBoxesPerWarp = (kWBoxes + kWProducers - 1) / kWProducers;
+static_assert(kWProducers >= 1 && kWBoxesPerWarp <= 32, "boxes per producer warp");
 constexpr int kWSoftmaxThreads = 256;
 constexpr int kWHalf = kWTok * 128;          // [64 tokens][64 d] bf16 = 8 KB
 constexpr int kWStageBytes = 4 * kWHalf;     // K halves, then V halves
-constexpr int kWQHalf = kWRows * 128;        // [128 rows][64 d] bf16 = 16 KB
-constexpr int kWQBytes = 2 * kWQHalf;
-constexpr int kWPBytes = kWRows * 128;       // one P buffer: [128 rows][64 keys] bf16
-constexpr int kWOffQ = 0;
-constexpr int kWOffP = kWOffQ + kWQBytes;
-constexpr int kWOffStage = kWOffP + 2 * kWPBytes;  // two P buffers
+constexpr int kWOffStage = 0;                // shared memory holds only the K/V ring
 constexpr int kWOffBar = kWOffStage + kWStages * kWStageBytes;
 constexpr int kWNumBars = 2 * kWStages + 2 + 2 + 2 + 2;  // full, empty, s_full, s_free, p_full, pv_done
 constexpr int kWSmemBytes = 1024 + kWOffBar + kWNumBars * 8 + 16;
-constexpr uint32_t kWTmemCols = 512;         // S buffers at 0 / 64, O buffers at 128 / 256
-constexpr uint32_t kWColO = 128;             // O of softmax group g at kWColO + 128 g
+static_assert(kWSmemBytes <= 227 * 1024, "K/V ring exceeds shared memory");
+// Tensor memory (512 columns x 128 lanes, lane = query row): fp32 scores
+// S[g] at 64 g, fp32 outputs O[g] at 128 + 128 g, bf16 probabilities P[g]
+// (64 keys packed in 32 columns) at 384 + 32 g, and the bf16 query rows Q
+// (128 d packed in 64 columns) at 448 -- the A operands of both MMAs.
+constexpr uint32_t kWTmemCols = 512;
+constexpr uint32_t kWColO = 128;
+constexpr uint32_t kWColP = 384;
+constexpr uint32_t kWColQ = 448;
 constexpr float kRescaleLog2 = 8.f;          // lazy rescale threshold (log2 units)
 
-// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
-// [rows][64 bf16] tile (the layout TMA writes and tcgen05 reads).
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
 // Tile j of a chunk goes to softmax group g = j & 1 (warps 4g..4g+3): its
-// scores land in TMEM buffer S[g], its probabilities in shared buffer P[g], and
+// scores land in TMEM buffer S[g], its probabilities in TMEM buffer P[g], and
 // P.V accumulates into O[g]; the two groups alternate, so one group's softmax
 // overlaps the other's, and their (m, l, O) merge exactly at the end.
 __global__ void __launch_bounds__(kWThreads, 1)
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kWStages; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], kWProducers);
       mbar_init(&empty_bar[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -142,8 +147,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const uint32_t smem_base = smem_addr(smem);
 
   // ============================================================ TMA producer
-  if (warp == kWProducerWarp) {
-    if (lane == 0) {
+  if (warp >= kWProducerWarp && warp < kWMmaWarp) {
+    const int pw_idx = warp - kWProducerWarp;
+    if (lane == 0 && pw_idx == 0) {
       prefetch_tensor_map(&k_map);
       prefetch_tensor_map(&v_map);
     }
@@ -165,25 +171,27 @@ __global__ void __launch_bounds__(kWThreads, 1)
         break;
       }
       const int tiles_here = min(kWTiles, n_tiles - it * kWTiles);
-      // page id of the tile this lane loads (lane / 4), picked in registers
+      // this lane's box: bx = lane * kWProducers + pw_idx (tile bx / 4; K or
+      // V and the d-half from bx % 4); page id of its tile picked in registers
+      const int bx = lane * kWProducers + pw_idx;
       int my_pg = 0;
 #pragma unroll
       for (int i = 0; i < kWTiles; ++i) {
         const int pg = a.paged ? pw.get(it * kWTiles + i) : 0;
-        if ((lane >> 2) == i) my_pg = pg;
+        if ((bx >> 2) == i) my_pg = pg;
       }
-      if (lane == 0)
-        mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(tiles_here * 4 * 2048));
+      // boxes of this warp that hold data (tiles past the chunk end are skipped)
+      int mine = 0;
+      for (int c = pw_idx; c < tiles_here * 4; c += kWProducers) ++mine;
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(mine * 2048));
       __syncwarp();
-      // one TMA box per lane (tile = lane / 4; K or V, d-half from lane % 4):
-      // a single thread issuing all of them serialises ~130 cycles per box
-      if (lane < tiles_here * 4) {
-        const int i = lane >> 2;
+      if (lane < kWBoxesPerWarp && bx < tiles_here * 4) {
+        const int i = bx >> 2;
         const int tok = t_begin + (it * kWTiles + i) * kTileTokens;
         const int grp = a.paged ? my_pg : b;
         const int tin = a.paged ? tok % a.page_size : tok;
-        const int half = lane & 1;
-        const bool is_v = (lane & 2) != 0;
+        const int half = bx & 1;
+        const bool is_v = (bx & 2) != 0;
         uint8_t* dst = smem + kWOffStage + s * kWStageBytes + (is_v ? 2 * kWHalf : 0) +
                        half * kWHalf + i * 2048;
         tma_load_4d(dst, is_v ? &v_map : &k_map, &full_bar[s], half * 64, kvh, tin, grp, policy);
@@ -200,78 +208,83 @@ __global__ void __launch_bounds__(kWThreads, 1)
   }
 
   // ============================================================= MMA issuer
+  // The whole warp runs this loop (all its values warp-uniform) and one
+  // elected lane issues each MMA and commit.
   if (warp == kWMmaWarp) {
-    named_barrier_sync(2, kWSoftmaxThreads + 32);  // Q is in shared memory
+    named_barrier_sync(2, kWSoftmaxThreads + 32);  // Q is in tensor memory
+    constexpr uint32_t kIdescQK = umma_idesc_bf16(kWRows, kWTok, false, false);
+    constexpr uint32_t kIdescPV = umma_idesc_bf16(kWRows, kHeadDim, false, true);
+    // B-operand descriptors of stage 0: other stages and K-steps differ only
+    // in the start-address field (16-byte units, no carry below 256 KB), so
+    // each MMA adds a constant to one of these. A (Q, P) is read from TMEM.
+    const uint64_t k_desc0 = umma_smem_desc(smem_base + kWOffStage, 16, 1024);
+    // B = V [64 keys][2 x 64 d], MN-major: d-halves 8 KB apart (LBO), 8-key
+    // groups 1 KB apart (SBO), 16 keys = 2 KB per K-step
+    const uint64_t v_desc0 = umma_smem_desc(smem_base + kWOffStage + 2 * kWHalf, kWHalf, 1024);
+    // O += P_jj . V_jj, then release the stage and the P buffer
+    auto issue_pv = [&](int jj) {
+      tc_fence_after_sync();
+      const uint32_t pa = tmem + kWColP + (jj & 1) * (kWTok / 2);
+      const uint64_t vd = v_desc0 + static_cast<uint64_t>((jj % kWStages) * (kWStageBytes >> 4));
+      const uint32_t d = tmem + kWColO + (jj & 1) * kHeadDim;
+#pragma unroll
+      for (int kk = 0; kk < kWTok / 16; ++kk)  // 16 keys = 8 P columns per K-step
+        umma_bf16_ts_warp(d, pa + kk * 8, vd + kk * (2048 >> 4), kIdescPV,
+                          (jj > 1 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(&pv_done[jj & 1]);
+      umma_commit_warp(&empty_bar[jj % kWStages]);
+    };
+    // S_j = Q . K_j^T: 16 d per K-step (8 Q columns; K: d-half kk / 4, 32
+    // bytes into its 128-byte swizzled rows)
+    auto issue_qk = [&](int j) {
+      tc_fence_after_sync();
+      const uint64_t kd = k_desc0 + static_cast<uint64_t>((j % kWStages) * (kWStageBytes >> 4));
+      const uint32_t d = tmem + (j & 1) * kWTok;
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk)
+        umma_bf16_ts_warp(d, tmem + kWColQ + kk * 8, kd + (((kk >> 2) * kWHalf + (kk & 3) * 32) >> 4),
+                          kIdescQK, kk > 0 ? 1u : 0u);
+      umma_commit_warp(&s_full[j & 1]);
+    };
+    // event loop: issue the next S = Q.K^T as soon as its stage has landed
+    // and its score buffer is free, and the next O += P.V as soon as its
+    // probabilities are ready -- neither waits on the other, so the two
+    // softmax groups overlap. A phase seen complete by any lane is complete.
     bool ok = true;
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = umma_idesc_bf16(kWRows, kWTok, false, false);
-      constexpr uint32_t kIdescPV = umma_idesc_bf16(kWRows, kHeadDim, false, true);
-      const uint32_t q_base = smem_base + kWOffQ;
-      const uint32_t p_base = smem_base + kWOffP;
-      // O += P_jj . V_jj, then release the stage and the P buffer
-      auto issue_pv_ready = [&](int jj) {
-        tc_fence_after_sync();
-        const uint32_t pb = p_base + (jj & 1) * kWPBytes;
-        const uint32_t v_base = smem_base + kWOffStage + (jj % kWStages) * kWStageBytes + 2 * kWHalf;
-#pragma unroll
-        for (int kk = 0; kk < kWTok / 16; ++kk) {
-          // A = P [128 rows][64 keys], K-major: 16 keys = 32 bytes per step
-          const uint64_t ad = umma_smem_desc(pb + kk * 32, 16, 1024);
-          // B = V [64 keys][2 x 64 d], MN-major: d-halves 8 KB apart (LBO),
-          // 8-key groups 1 KB apart (SBO), 16 keys = 2 KB per step
-          const uint64_t bd = umma_smem_desc(v_base + kk * 2048, kWHalf, 1024);
-          umma_bf16_ss(tmem + kWColO + (jj & 1) * kHeadDim, ad, bd, kIdescPV,
-                       (jj > 1 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&pv_done[jj & 1]);
-        umma_commit(&empty_bar[jj % kWStages]);
-      };
-      // event loop: issue the next S = Q.K^T as soon as its stage has landed
-      // and its score buffer is free, and the next O += P.V as soon as its
-      // probabilities are ready -- neither waits on the other, so the two
-      // softmax groups overlap
-      auto issue_qk = [&](int j) {
-        tc_fence_after_sync();
-        const int buf = j & 1;
-        const uint32_t k_base = smem_base + kWOffStage + (j % kWStages) * kWStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          // 16 d per step: half kk/4, 32 bytes into the 128-byte swizzled row
-          const uint64_t ad = umma_smem_desc(q_base + (kk >> 2) * kWQHalf + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_smem_desc(k_base + (kk >> 2) * kWHalf + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + buf * kWTok, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[buf]);
-      };
-      int next_qk = 0, next_pv = 0;
-      unsigned long long idle_since = 0;
-      while (next_pv < n_iters) {
-        bool progress = false;
-        if (next_qk < n_iters) {
-          const int j = next_qk;
-          if (mbar_test(&full_bar[j % kWStages], (j / kWStages) & 1) &&
-              (j < 2 || mbar_test(&s_free[j & 1], ((j >> 1) - 1) & 1))) {
-            issue_qk(j);
-            ++next_qk;
-            progress = true;
-          }
-        }
-        if (next_pv < next_qk && mbar_test(&p_full[next_pv & 1], (next_pv >> 1) & 1)) {
-          issue_pv_ready(next_pv);
-          ++next_pv;
+    int next_qk = 0, next_pv = 0;
+    unsigned long long idle_since = 0;
+    while (next_pv < n_iters) {
+      bool progress = false;
+      if (next_qk < n_iters) {
+        const int j = next_qk;
+        const bool landed = mbar_test(&full_bar[j % kWStages], (j / kWStages) & 1);
+        const bool s_ready = j < 2 || mbar_test(&s_free[j & 1], ((j >> 1) - 1) & 1);
+        if (__any_sync(kFull, landed) && __any_sync(kFull, s_ready)) {
+          issue_qk(j);
+          ++next_qk;
           progress = true;
         }
-        if (progress) {
-          idle_since = 0;
-        } else if (idle_since == 0) {
-          idle_since = global_timer_ns();
-        } else if (global_timer_ns() - idle_since > kWaitLimitNs) {
+      }
+      if (next_pv < next_qk &&
+          __any_sync(kFull, mbar_test(&p_full[next_pv & 1], (next_pv >> 1) & 1))) {
+        issue_pv(next_pv);
+        ++next_pv;
+        progress = true;
+      }
+      if (progress) {
+        idle_since = 0;
+      } else {
+        const unsigned long long now = __shfl_sync(kFull, global_timer_ns(), 0);
+        if (idle_since == 0) {
+          idle_since = now;
+        } else if (now - idle_since > kWaitLimitNs) {
           ok = false;
           break;
         }
       }
-      if (!ok && a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
     }
+    if (!ok && lane == 0 && a.status != nullptr)
+      atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
     __syncwarp();
     named_barrier_sync(3, kWSoftmaxThreads + 32);  // softmax warps are done with TMEM
     tc_fence_after_sync();
@@ -289,7 +302,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const int t = r / a.group;
     lim = a.causal ? min(t_end, L - a.q_len + 1 + t) : t_end;
   }
-  // ---- Q rows into shared memory as the K-major swizzled A operand
+  // ---- this thread's query row (zeros for padding rows) into TMEM lane r:
+  // the A operand of S = Q.K^T, d pairs packed in 64 columns
   if (grp == 0) {
     const uint16_t* qrow = nullptr;
     if (r < a.rows) {
@@ -299,12 +313,22 @@ __global__ void __launch_bounds__(kWThreads, 1)
              static_cast<int64_t>(kvh * a.group + g) * a.q_sh;
     }
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 v = qrow ? *reinterpret_cast<const uint4*>(qrow + c * 8) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(smem + kWOffQ + (c >> 3) * kWQHalf + sw128(r, c & 7)) = v;
+    for (int half = 0; half < 2; ++half) {
+      float w[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = qrow ? *reinterpret_cast<const uint4*>(qrow + half * 64 + c * 8)
+                             : make_uint4(0, 0, 0, 0);
+        w[4 * c] = __uint_as_float(v.x);
+        w[4 * c + 1] = __uint_as_float(v.y);
+        w[4 * c + 2] = __uint_as_float(v.z);
+        w[4 * c + 3] = __uint_as_float(v.w);
+      }
+      tmem_st32(lane_base + kWColQ + half * 32, w);
     }
-    fence_proxy_async_smem();
+    tmem_wait_st();
   }
+  tc_fence_before_sync();
   named_barrier_sync(2, kWSoftmaxThreads + 32);
 
   float m_used = -INFINITY;  // reference max of P (log2 domain), raised lazily
@@ -383,11 +407,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
         tmem_wait_st();
       }
     }
-    // P row (64 bf16 = 8 chunks) into the swizzled A operand of P.V
+    // P row (64 bf16 packed in 32 columns) into TMEM: the A operand of P.V
+    {
+      float w[32];
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      *reinterpret_cast<uint4*>(smem + kWOffP + grp * kWPBytes + sw128(r, c)) =
-          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int i = 0; i < 32; ++i) w[i] = __uint_as_float(pk[i]);
+      tmem_st32(lane_base + kWColP + grp * (kWTok / 2), w);
+    }
     // keys past the chunk end: their V rows may hold anything (NaN * 0 is
     // NaN), so zero them before the MMA reads the stage
     const int n_valid = min(kWTok, t_end - tok0);
@@ -400,7 +426,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
             make_uint4(0, 0, 0, 0);
       }
     }
-    fence_proxy_async_smem();
+    if (n_valid < kWTok) fence_proxy_async_smem();
+    tmem_wait_st();
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(&p_full[grp]);
@@ -416,7 +443,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   // ---- merge the two groups (same recurrence as the combine) and write
   // O / l (final bf16 row or fp32 partial) and the LSE; group g writes the
   // d-columns [64 g, 64 g + 64) of every row
-  float* stat = reinterpret_cast<float*>(smem + kWOffP);  // P buffers are idle now
+  float* stat = reinterpret_cast<float*>(smem + kWOffStage);  // the K/V ring is idle now
   tc_fence_before_sync();
   named_barrier_sync(4, kWSoftmaxThreads);  // both groups' last P.V are done
   stat[grp * 256 + r] = m_used;
