@@ -33,6 +33,7 @@ struct SplitArgs {
   int max_seq_len, chunk_len, num_splits;
   int causal;
   float scale_log2;                    // softmax scale * log2(e)
+  int persistent;                      // wide kernel: CTAs walk an item list (set by its launcher)
 };
 
 struct CombineArgs {

@@ -167,3 +167,21 @@ def test_cluster_merge_is_one_launch_and_matches_two_pass(binding):
         assert_out_close(bf16_tensor_to_f64(o1), bf16_tensor_to_f64(o2), what="cluster vs two-pass")
     # beyond the largest cluster (after rounding the chunk length to 16 tokens)
     assert binding.decode_attn_launch_count(p, 40) == 2
+
+
+@pytest.mark.parametrize("batch", [3, 300, 1030])
+def test_wide_schedule_batch_sizes(binding, batch):
+    """The tcgen05 kernel's persistent schedule over batches of every kind:
+    few requests (partial chunks sorted by length), more than the sorting
+    limit (index order), and more than its tables hold (one item per CTA);
+    lengths include empty requests, full and partial chunks."""
+    rng = np.random.default_rng(40 + batch)
+    lens = rng.integers(4, 200, batch).astype(np.int32)  # causal: at least q_len keys
+    lens[:: 7] = 0
+    lens[1:: 11] = 160  # two full 80-token chunks at 3 splits
+    shp = W.small_shape("wide_sched", batch=batch, q_len=4, num_q_heads=16, num_kv_heads=2,
+                        lo=0, hi=200, paged=True, causal=True, seed=41 + batch)
+    inp = W.make_host_inputs(shp, seq_lens=lens)
+    for S in (1, 3):
+        out, lse = check(binding, inp, S)
+        assert np.all(bf16_tensor_to_f64(out)[lens == 0] == 0)
