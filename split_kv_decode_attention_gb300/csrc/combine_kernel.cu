@@ -19,43 +19,49 @@ namespace dattn {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kBlocksPerSm = 6;  // registers capped so that 48 warps fit per SM
 constexpr float kLog2e = 1.4426950408889634f;
 
-__global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(32 * kWarpsPerBlock, kBlocksPerSm)
+    combine_kernel(const CombineArgs a) {
   constexpr uint32_t kFull = 0xffffffffu;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
+  const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.num_q_heads;
+  const bool live = row < nrows;
+  const int h = live ? static_cast<int>(row % a.num_q_heads) : 0;
+  const int t = live ? static_cast<int>((row / a.num_q_heads) % a.q_len) : 0;
+  const int b = live ? static_cast<int>(row / (static_cast<int64_t>(a.num_q_heads) * a.q_len)) : 0;
+  const int S = a.num_splits;
+  const float* pl = a.part_lse + row * S;
+  const float* po = a.part_o + row * S * kHeadDim + lane * 4;
   // the split kernel that wrote the partials may still be running (this
   // kernel may launch during its tail): wait before reading anything
   grid_dependency_wait();
-  const int64_t nrows = static_cast<int64_t>(a.batch) * a.q_len * a.num_q_heads;
-  if (row >= nrows) return;
-  const int h = static_cast<int>(row % a.num_q_heads);
-  const int t = static_cast<int>((row / a.num_q_heads) % a.q_len);
-  const int b = static_cast<int>(row / (static_cast<int64_t>(a.num_q_heads) * a.q_len));
+  if (!live) return;
+
+  // one round trip for the request length, the first 32 LSEs and the first
+  // kBatch partial rows: none of these loads depends on another. Splits past
+  // the request's chunk count hold stale values, dropped by the selects below.
+  constexpr int kBatch = 4;
+  const uint64_t dead = l2_evict_first_policy();  // each partial is read once
   int L = a.seq_lens[b];
+  const float lse0 = lane < S ? ld_global_hint1(pl + lane, dead) : -INFINITY;
+  float4 v[kBatch];
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j)
+    v[j] = j < S ? ld_global_hint(po + static_cast<int64_t>(j) * kHeadDim, dead)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
   L = L < 0 ? 0 : (L > a.max_seq_len ? a.max_seq_len : L);
   const int n = L > 0 ? (L + a.chunk_len - 1) / a.chunk_len : 1;
   if (n < 2) return;  // the split kernel wrote this row directly
 
-  const int S = a.num_splits;
-  const float* pl = a.part_lse + row * S;
-  const float* po = a.part_o + row * S * kHeadDim + lane * 4;
   uint16_t* orow = a.out + static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(t) * a.o_st +
                    static_cast<int64_t>(h) * a.o_sh + lane * 4;
-
-  // splits in groups of 32: lane j holds lse of split s0 + j; the group's
-  // partial rows are loaded kBatch at a time, the first batch in the same
-  // round trip as the LSEs (the loads do not depend on the weights)
-  constexpr int kBatch = 8;
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, pl[s]);
-  float4 v[kBatch];
-#pragma unroll
-  for (int j = 0; j < kBatch; ++j)
-    v[j] = j < n ? *reinterpret_cast<const float4*>(po + static_cast<int64_t>(j) * kHeadDim)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  // splits in groups of 32: lane j holds lse of split s0 + j
+  float M = lane < n ? lse0 : -INFINITY;
+  for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, ld_global_hint1(pl + s, dead));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 16));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 8));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 4));
@@ -70,23 +76,25 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(const Comb
   float W = 0.f;
   for (int s0 = 0; s0 < n; s0 += 32) {
     const int cnt = min(32, n - s0);
-    const float w_mine = lane < cnt ? ex2((pl[s0 + lane] - M) * kLog2e) : 0.f;
+    const float lse_mine = s0 == 0 ? lse0 : (lane < cnt ? ld_global_hint1(pl + s0 + lane, dead) : -INFINITY);
+    const float w_mine = lane < cnt ? ex2((lse_mine - M) * kLog2e) : 0.f;
     for (int j0 = 0; j0 < cnt; j0 += kBatch) {
       if (s0 + j0 > 0) {  // batch 0 of group 0 is already in flight
 #pragma unroll
         for (int j = 0; j < kBatch; ++j)
-          v[j] = j0 + j < cnt ? *reinterpret_cast<const float4*>(
-                                    po + static_cast<int64_t>(s0 + j0 + j) * kHeadDim)
+          v[j] = j0 + j < cnt ? ld_global_hint(po + static_cast<int64_t>(s0 + j0 + j) * kHeadDim, dead)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
-        const float w = __shfl_sync(kFull, w_mine, (j0 + j) & 31);
-        W += w;
-        acc.x += w * v[j].x;
-        acc.y += w * v[j].y;
-        acc.z += w * v[j].z;
-        acc.w += w * v[j].w;
+        if (j0 + j < cnt) {  // (not a multiply by zero: stale values may be NaN)
+          const float w = __shfl_sync(kFull, w_mine, (j0 + j) & 31);
+          W += w;
+          acc.x += w * v[j].x;
+          acc.y += w * v[j].y;
+          acc.z += w * v[j].z;
+          acc.w += w * v[j].w;
+        }
       }
     }
   }

@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
                                   static_cast<int64_t>(h) * a.o_sh + d) = pk;
       } else {
         const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
-        *reinterpret_cast<float4*>(a.part_o + (prow * S + split) * kHeadDim + d) = v;
+        st_global_hint(a.part_o + (prow * S + split) * kHeadDim + d, v, l2_evict_last_policy());
       }
     }
     if (threadIdx.x < a.rows) {
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
       if (direct)
         a.lse[prow] = lse;
       else
-        a.part_lse[prow * S + split] = lse;
+        st_global_hint(a.part_lse + prow * S + split, lse, l2_evict_last_policy());
     }
   }
 }

@@ -55,7 +55,7 @@ constexpr int kWTiles = kWTok / kTileTokens; // 16-token page tiles per stage
 #endif
 constexpr int kWStages = DATTN_WIDE_STAGES;  // K/V stages in flight
 #ifndef DATTN_WIDE_PRODUCERS
-#define DATTN_WIDE_PRODUCERS 4
+#define DATTN_WIDE_PRODUCERS 5
 #endif
 // TMA copies issued by one warp are serialised (~130 cycles per box), so
 // several producer warps share each stage's boxes.
@@ -742,9 +742,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                            pack_bf16x2(o[i + 4], o[i + 5]), pack_bf16x2(o[i + 6], o[i + 7]));
         } else {
           float* dst = a.part_o + (prow * S + it.split) * kHeadDim + d0;
+          const uint64_t keep = l2_evict_last_policy();
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+            st_global_hint(dst + i, make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]), keep);
         }
       }
     }
@@ -753,7 +754,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (direct)
         a.lse[prow] = lse;
       else
-        a.part_lse[prow * S + it.split] = lse;
+        st_global_hint(a.part_lse + prow * S + it.split, lse, l2_evict_last_policy());
     }
     if (!ok) break;
   }
