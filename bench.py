@@ -208,9 +208,9 @@ class Dist:
 
 def algorithmic_bytes(shape, seq_lens: np.ndarray, direct_rows: bool = True) -> dict:
     """Bytes one call must move at minimum: K+V of every valid token per KV
-    head, q, out (bf16), lse (fp32) and the block-table entries used."""
+    head (bf16 or FP8), q, out (bf16), lse (fp32) and the block-table entries used."""
     lens = seq_lens.astype(np.int64)
-    kv = int(lens.sum()) * shape.num_kv_heads * shape.head_dim * 2 * 2
+    kv = int(lens.sum()) * shape.num_kv_heads * shape.head_dim * 2 * W.kv_elem_bytes(shape)
     rows = shape.batch * shape.q_len * shape.num_q_heads
     q_out = rows * shape.head_dim * 2 * 2 + rows * 4
     bt = int(((lens + shape.page_size - 1) // shape.page_size).sum()) * 4 if shape.paged else 0
@@ -260,12 +260,15 @@ def host_copy(inp_dev):
     import torch
 
     def bits(t):
+        if t.element_size() == 1:   # FP8 E4M3 bytes
+            return t.contiguous().cpu().numpy().view(np.uint8)
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
     bt = None if inp_dev.block_table is None else inp_dev.block_table.cpu().numpy()
     return W.DecodeInputs(inp_dev.shape, bits(inp_dev.q), bits(inp_dev.k_cache),
                           bits(inp_dev.v_cache), bt, inp_dev.seq_lens.cpu().numpy(),
-                          inp_dev.max_seq_len, inp_dev.num_pages, inp_dev.page_size)
+                          inp_dev.max_seq_len, inp_dev.num_pages, inp_dev.page_size,
+                          inp_dev.k_scale, inp_dev.v_scale)
 
 
 # ---------------------------------------------------------------- our arm
@@ -290,7 +293,8 @@ def run_ours(args, dist: "Dist"):
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len,
-                                    causal=shape.causal, scale=shape.scale, out=out)
+                                    causal=shape.causal, scale=shape.scale, out=out,
+                                    k_scale=inp.k_scale, v_scale=inp.v_scale)
     if args.num_splits > 0:
         S = args.num_splits
     else:
@@ -385,14 +389,16 @@ def run_ours(args, dist: "Dist"):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_all, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16 (FP8 E4M3 K/V widened)" if shape.kv_fp8 else "bf16",
+        "data": "synthetic",
         "us_per_call": round(ms_all * 1e3, 2),
         "us_per_call_median": round(float(np.median(call_ms)) * 1e3, 2),
         "us_per_call_p10_p90": [round(float(np.percentile(call_ms, 10)) * 1e3, 2),
                                 round(float(np.percentile(call_ms, 90)) * 1e3, 2)],
         "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
         "us_per_call_single_decode_attn": round(fused_us, 2),
-        "config": {"workload": args.workload, "batch": shape.batch, "q_len": shape.q_len,
+        "config": {"workload": args.workload, "kv_dtype": "fp8_e4m3" if shape.kv_fp8 else "bf16",
+                   "batch": shape.batch, "q_len": shape.q_len,
                    "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
                    "head_dim": shape.head_dim, "seq_lens": [int(lens_h.min()), int(lens_h.max())],
                    "paged": shape.paged, "page_size": shape.page_size if shape.paged else None,

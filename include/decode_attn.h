@@ -40,6 +40,15 @@
  * Strides are in elements; K and V base pointers must be 16-byte aligned and
  * every KV stride a multiple of 8 elements (16 bytes).
  *
+ * FP8 caches (flags & DA_FLAG_KV_FP8_E4M3).  K and V hold one byte per element
+ * in the OCP FP8 E4M3 format (1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits, subnormals, no infinities, S.1111.111 = NaN) with one fp32
+ * scale per cache: the keys and values are k_scale * K and v_scale * V
+ * (quantisation with explicit scaling factors rather than a plain cast:
+ * "Capstone FlashAttention", §2.2 FP8 with scaling; the CUTLASS split-KV post,
+ * §5.8).  q, out and lse keep their types.  Strides are then in bytes and must
+ * be multiples of 16; at most 16 rows per kv head ((Hq/Hkv)*q_len).
+ *
  * Ownership and errors.  The caller owns every buffer (device memory unless
  * stated otherwise), including the workspace.  The library allocates nothing
  * on the device, never synchronises the stream and may be captured in a CUDA
@@ -82,6 +91,8 @@ extern "C" {
 #define DA_ERR_NO_DEVICE -9        /* no usable sm_103 device is current */
 #define DA_ERR_SPLITS -10          /* num_splits out of range */
 #define DA_ERR_STATIC_WORKSPACE_LIMIT -11 /* partials exceed the static workspace */
+#define DA_ERR_UNSUPPORTED -12     /* a flag combination this library does not run:
+                                      FP8 caches with more than 16 rows per kv head */
 
 /* size of the device array behind decode_attn_static_workspace() */
 #define DECODE_ATTN_STATIC_WORKSPACE_BYTES (16u << 20)
@@ -90,6 +101,8 @@ extern "C" {
 #define DA_FLAG_TWO_PASS 1u        /* always write fp32 partials to the workspace and
                                       merge them with the combine kernel (no
                                       cluster merge); needed to read partials */
+#define DA_FLAG_KV_FP8_E4M3 2u     /* K and V caches are FP8 E4M3 bytes scaled by
+                                      k_scale / v_scale (see "FP8 caches" above) */
 
 /* device status bits (OR-ed into *status) */
 #define DA_STATUS_BAD_PAGE 1u      /* block-table entry outside [0, num_pages) */
@@ -123,13 +136,16 @@ typedef struct decode_attn_params {
   int64_t kv_stride_token;
   int64_t kv_stride_head;
   int64_t block_table_stride; /* elements between rows of block_table */
+  float k_scale;              /* FP8 caches: keys = k_scale * K (1 by default) */
+  float v_scale;              /* FP8 caches: values = v_scale * V (1 by default) */
 } decode_attn_params;
 
 /*
  * Fill *p with the strides of densely packed tensors:
  *   q, out [B, q_len, Hq, D]; paged caches [num_pages, page_size, Hkv, D];
  *   contiguous caches [B, max_seq_len, Hkv, D]; block_table [B, max_pages].
- * scale = 1/sqrt(head_dim).  Pass page_size = 0 for a contiguous cache.
+ * scale = 1/sqrt(head_dim), k_scale = v_scale = 1, flags = 0 (bf16 caches).
+ * Pass page_size = 0 for a contiguous cache.
  */
 void decode_attn_params_init(decode_attn_params *p, int32_t batch, int32_t q_len,
                              int32_t num_q_heads, int32_t num_kv_heads,

@@ -10,7 +10,11 @@ Functions
 decode_attention(inputs, ...)  exact softmax(q.K^T*scale).V per query head
                                ("Capstone FlashAttention", §1.1 formula; §1.2
                                three-pass safe softmax), gathered through the
-                               block table (§4.1), GQA kvh = h // G (§4.2).
+                               block table (§4.1), GQA kvh = h // G (§4.2);
+                               bf16 caches, or FP8 E4M3 caches with one scale
+                               each (§2.2 FP8 with scaling factors).
+e4m3_values()                  the 256 E4M3 codes decoded by the oracle's own
+                               decoder (written from the format definition).
 merge_partials(part_out, part_lse)
                                combine of normalised chunk results by their
                                log-sum-exps ("Capstone FlashAttention", §1.2
@@ -55,10 +59,12 @@ def _load():
         vp = ctypes.c_void_p
         lib.oracle_decode_attn.argtypes = [
             i32, i32, i32, i32, i32, vp, vp, vp, i64, i64, i64, i32, vp, i64,
-            i32, i32, i32, vp, dbl, i32, i64, i64, vp, i64, vp, vp, i32]
+            i32, i32, i32, vp, dbl, i32, i64, i64, vp, i64, vp, vp, i32, i32, dbl, dbl]
         lib.oracle_decode_attn.restype = i32
         lib.oracle_merge_partials.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
         lib.oracle_merge_partials.restype = i32
+        lib.oracle_e4m3_table.argtypes = [vp]
+        lib.oracle_e4m3_table.restype = None
         _lib = lib
     return _lib
 
@@ -78,12 +84,14 @@ def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                      scale: Optional[float] = None, causal: bool = False,
                      key_lo: int = 0, key_hi: int = 2**62,
                      rows: Optional[np.ndarray] = None,
-                     threads: Optional[int] = None):
+                     threads: Optional[int] = None,
+                     kv_fp8: bool = False, k_scale: float = 1.0, v_scale: float = 1.0):
     """Exact attention in fp64.
 
     q        uint16 bf16 bits [B, q_len, Hq, D]
-    k/v      uint16 bf16 bits, paged [P, page_size, Hkv, D] (block_table given)
-             or contiguous [B, capacity, Hkv, D] (block_table None)
+    k/v      uint16 bf16 bits (or uint8 E4M3 bytes with kv_fp8: keys =
+             k_scale * K, values = v_scale * V), paged [P, page_size, Hkv, D]
+             (block_table given) or contiguous [B, capacity, Hkv, D]
     seq_lens int32 [B]
     rows     optional flat row ids (b*q_len + t)*Hq + h to compute
     Returns (out float64 [B, q_len, Hq, D] or [len(rows), D],
@@ -91,8 +99,9 @@ def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
     """
     q = np.ascontiguousarray(q, dtype=np.uint16)
     B, T, Hq, D = q.shape
-    if k_cache.dtype != np.uint16 or v_cache.dtype != np.uint16:
-        raise TypeError("k/v caches must be bf16 bit patterns (uint16)")
+    want = np.uint8 if kv_fp8 else np.uint16
+    if k_cache.dtype != want or v_cache.dtype != want:
+        raise TypeError("k/v caches must be bf16 bit patterns (uint16) or E4M3 bytes (uint8, kv_fp8)")
     if k_cache.shape != v_cache.shape or k_cache.shape[2] != num_kv_heads:
         raise ValueError("k/v cache shapes disagree")
     for a in (k_cache, v_cache):
@@ -128,7 +137,8 @@ def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
         slots * hkv * D, hkv * D, D, page_size, _ptr(block_table), bt_stride,
         max_pages, num_pages, capacity, _ptr(seq_lens), float(scale),
         1 if causal else 0, int(key_lo), int(key_hi), _ptr(rows), n,
-        _ptr(out), _ptr(lse), threads or default_threads())
+        _ptr(out), _ptr(lse), threads or default_threads(),
+        1 if kv_fp8 else 0, float(k_scale), float(v_scale))
     if rc != 0:
         raise ValueError(f"oracle_decode_attn failed with code {rc} "
                          "(-2: block table entry out of range, -3: token beyond capacity)")
@@ -144,7 +154,15 @@ def decode_attention_inputs(inp, *, rows=None, key_lo=0, key_hi=2**62,
         num_kv_heads=s.num_kv_heads, block_table=inp.block_table,
         page_size=inp.page_size, num_pages=inp.num_pages, scale=s.scale,
         causal=s.causal, key_lo=key_lo, key_hi=key_hi, rows=rows,
-        threads=threads)
+        threads=threads, kv_fp8=getattr(s, "kv_fp8", False),
+        k_scale=getattr(inp, "k_scale", 1.0), v_scale=getattr(inp, "v_scale", 1.0))
+
+
+def e4m3_values() -> np.ndarray:
+    """float64 [256]: code c decoded by the oracle (NaN for S.1111.111)."""
+    out = np.zeros(256, dtype=np.float64)
+    _load().oracle_e4m3_table(_ptr(out))
+    return out
 
 
 def merge_partials(part_out: np.ndarray, part_lse: np.ndarray,

@@ -34,6 +34,13 @@
  * lse = M + ln(sum w_s) -- the two-block merge of running max / running sum
  * ("Capstone FlashAttention", §1.2 formal proof; §2.3 FlashDecoding reduce).
  *
+ * FP8 caches (kv_fp8 != 0): K and V hold one byte per element in the OCP
+ * FP8 E4M3 format and the keys / values are k_scale * K and v_scale * V
+ * (quantisation with explicit scaling factors: "Capstone FlashAttention",
+ * §2.2 FP8 with scaling; the CUTLASS split-KV post, §5.8).  The byte is
+ * decoded from the format's definition (e4m3_to_double) and everything else
+ * is the same definition in fp64.
+ *
  * Threads split the independent (b, t, h) rows; each row is computed start to
  * finish by one thread with no reordering beyond the definition.
  */
@@ -56,10 +63,23 @@ static double bf16_to_double(uint16_t bits) {
   return (double)f;
 }
 
+/* OCP FP8 E4M3: sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+ * Exponent field 0 holds the subnormals (m/8) * 2^(1-7) = m * 2^-9; fields
+ * 1..15 the normals (1 + m/8) * 2^(e-7) = (8 + m) * 2^(e-10); there are no
+ * infinities and S.1111.111 is NaN (so the largest value is 1.75 * 2^8 = 448). */
+static double e4m3_to_double(uint8_t x) {
+  const int sign = x >> 7, e = (x >> 3) & 15, m = x & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+  return sign ? -v : v;
+}
+
 typedef struct {
   int batch, q_len, num_q_heads, num_kv_heads, head_dim;
   const uint16_t *q;              /* [B, q_len, Hq, D] contiguous */
-  const uint16_t *k, *v;          /* caches, element strides below */
+  const void *k, *v;              /* caches (bf16 bits or E4M3 bytes), element strides below */
+  int kv_fp8;                     /* caches hold E4M3 bytes scaled by k_scale / v_scale */
+  double k_scale, v_scale;
   int64_t stride_page, stride_tok, stride_head;
   int page_size;                  /* paged: tokens per page */
   const int32_t *block_table;     /* NULL: contiguous, request b = "page" b */
@@ -83,24 +103,28 @@ typedef struct {
   int error;
 } oracle_worker;
 
-/* Address of token j's key (or value) row for request b and head kvh, or
- * NULL with *err set when the block table / capacity does not cover it. */
-static const uint16_t *kv_row(const oracle_job *J, const uint16_t *base, int b,
-                              int64_t j, int kvh, int *err) {
+/* Element offset of token j's key (or value) row for request b and head kvh,
+ * or -1 with *err set when the block table / capacity does not cover it. */
+static int64_t kv_row(const oracle_job *J, int b, int64_t j, int kvh, int *err) {
   int64_t page, slot;
   if (J->block_table) {
     int64_t col = j / J->page_size;
-    if (col >= J->max_pages_per_seq) { *err = ORACLE_ERR_RANGE; return NULL; }
+    if (col >= J->max_pages_per_seq) { *err = ORACLE_ERR_RANGE; return -1; }
     page = J->block_table[(int64_t)b * J->bt_stride + col];
-    if (page < 0 || page >= J->num_pages) { *err = ORACLE_ERR_PAGE; return NULL; }
+    if (page < 0 || page >= J->num_pages) { *err = ORACLE_ERR_PAGE; return -1; }
     slot = j % J->page_size;
   } else {
-    if (j >= J->capacity) { *err = ORACLE_ERR_RANGE; return NULL; }
+    if (j >= J->capacity) { *err = ORACLE_ERR_RANGE; return -1; }
     page = b;
     slot = j;
   }
-  return base + page * J->stride_page + slot * J->stride_tok +
-         (int64_t)kvh * J->stride_head;
+  return page * J->stride_page + slot * J->stride_tok + (int64_t)kvh * J->stride_head;
+}
+
+/* Element `e` of a cache as a real number. */
+static double kv_value(const oracle_job *J, const void *base, double scale, int64_t e) {
+  if (J->kv_fp8) return scale * e4m3_to_double(((const uint8_t *)base)[e]);
+  return bf16_to_double(((const uint16_t *)base)[e]);
 }
 
 static int one_row(const oracle_job *J, int64_t flat, double *o, double *lse_out) {
@@ -130,10 +154,10 @@ static int one_row(const oracle_job *J, int64_t flat, double *o, double *lse_out
   /* pass 1: scores and their maximum */
   double m = -INFINITY;
   for (int64_t j = lo; j < hi; ++j) {
-    const uint16_t *kr = kv_row(J, J->k, b, j, kvh, &err);
-    if (!kr) { free(qd); free(s); return err; }
+    const int64_t kr = kv_row(J, b, j, kvh, &err);
+    if (kr < 0) { free(qd); free(s); return err; }
     double acc = 0.0;
-    for (int d = 0; d < D; ++d) acc += qd[d] * bf16_to_double(kr[d]);
+    for (int d = 0; d < D; ++d) acc += qd[d] * kv_value(J, J->k, J->k_scale, kr + d);
     s[j - lo] = J->scale * acc;
     if (s[j - lo] > m) m = s[j - lo];
   }
@@ -143,9 +167,9 @@ static int one_row(const oracle_job *J, int64_t flat, double *o, double *lse_out
   /* pass 3: normalised weights times values */
   for (int64_t j = lo; j < hi; ++j) {
     const double p = exp(s[j - lo] - m) / l;
-    const uint16_t *vr = kv_row(J, J->v, b, j, kvh, &err);
-    if (!vr) { free(qd); free(s); return err; }
-    for (int d = 0; d < D; ++d) o[d] += p * bf16_to_double(vr[d]);
+    const int64_t vr = kv_row(J, b, j, kvh, &err);
+    if (vr < 0) { free(qd); free(s); return err; }
+    for (int d = 0; d < D; ++d) o[d] += p * kv_value(J, J->v, J->v_scale, vr + d);
   }
   *lse_out = m + log(l);
   free(qd);
@@ -169,8 +193,11 @@ static void *worker_main(void *arg) {
 /*
  * Exact decode attention in fp64.
  *   q                 bf16 bits [B, q_len, Hq, D], contiguous
- *   k, v              bf16 bits; element (page, slot, head, d) at
+ *   k, v              bf16 bits (uint16), or E4M3 bytes when kv_fp8; element
+ *                     (page, slot, head, d) at
  *                     page*stride_page + slot*stride_tok + head*stride_head + d
+ *   kv_fp8, k_scale, v_scale
+ *                     FP8 caches: keys = k_scale * K, values = v_scale * V
  *   block_table       int32 [B, bt_stride] (first max_pages_per_seq used), or
  *                     NULL for a contiguous cache where "page" = request and
  *                     capacity = tokens per request
@@ -180,14 +207,15 @@ static void *worker_main(void *arg) {
  * Returns 0, or a negative code when an index leaves the cache.
  */
 int oracle_decode_attn(int batch, int q_len, int num_q_heads, int num_kv_heads,
-                       int head_dim, const uint16_t *q, const uint16_t *k,
-                       const uint16_t *v, int64_t stride_page, int64_t stride_tok,
+                       int head_dim, const uint16_t *q, const void *k,
+                       const void *v, int64_t stride_page, int64_t stride_tok,
                        int64_t stride_head, int page_size,
                        const int32_t *block_table, int64_t bt_stride,
                        int max_pages_per_seq, int num_pages, int capacity,
                        const int32_t *seq_lens, double scale, int causal,
                        int64_t key_lo, int64_t key_hi, const int32_t *rows,
-                       int64_t nrows, double *out, double *lse, int nthreads) {
+                       int64_t nrows, double *out, double *lse, int nthreads,
+                       int kv_fp8, double k_scale, double v_scale) {
   if (batch < 0 || q_len < 1 || num_q_heads < 1 || num_kv_heads < 1 ||
       num_q_heads % num_kv_heads != 0 || head_dim < 1 || !q || !k || !v ||
       !seq_lens || !out || !lse)
@@ -198,6 +226,7 @@ int oracle_decode_attn(int batch, int q_len, int num_q_heads, int num_kv_heads,
   J.batch = batch; J.q_len = q_len; J.num_q_heads = num_q_heads;
   J.num_kv_heads = num_kv_heads; J.head_dim = head_dim;
   J.q = q; J.k = k; J.v = v;
+  J.kv_fp8 = kv_fp8; J.k_scale = k_scale; J.v_scale = v_scale;
   J.stride_page = stride_page; J.stride_tok = stride_tok; J.stride_head = stride_head;
   J.page_size = page_size; J.block_table = block_table; J.bt_stride = bt_stride;
   J.max_pages_per_seq = max_pages_per_seq; J.num_pages = num_pages;
@@ -272,4 +301,9 @@ int oracle_merge_partials(int64_t nrows, int nsplit, int head_dim,
     lse[r] = M + log(W);
   }
   return ORACLE_OK;
+}
+
+/* The oracle's E4M3 decoding of every code, for its pins. */
+void oracle_e4m3_table(double *out) {
+  for (int c = 0; c < 256; ++c) out[c] = e4m3_to_double((uint8_t)c);
 }

@@ -25,6 +25,8 @@ DA_STATUS_SEQ_LEN = 2
 DA_STATUS_SHORT_CAUSAL = 4
 DA_STATUS_TIMEOUT = 8
 DA_FLAG_TWO_PASS = 1
+DA_FLAG_KV_FP8_E4M3 = 2
+DA_ERR_UNSUPPORTED = -12
 
 EXPORTED_SYMBOLS = (
     "decode_attn_params_init", "decode_attn_plan", "decode_attn_chunk_len",
@@ -50,6 +52,7 @@ class DecodeAttnParams(ctypes.Structure):
         ("o_stride_token", ctypes.c_int64), ("o_stride_head", ctypes.c_int64),
         ("kv_stride_page", ctypes.c_int64), ("kv_stride_token", ctypes.c_int64),
         ("kv_stride_head", ctypes.c_int64), ("block_table_stride", ctypes.c_int64),
+        ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
     ]
 
 
@@ -127,10 +130,12 @@ def decode_attn_params_init(batch: int, q_len: int, num_q_heads: int, num_kv_hea
 
 def params_from_tensors(q, k_cache, block_table=None, *, max_seq_len: int,
                         causal: bool = False, scale: Optional[float] = None,
-                        out=None, two_pass: bool = False) -> DecodeAttnParams:
+                        out=None, two_pass: bool = False, k_scale: float = 1.0,
+                        v_scale: float = 1.0) -> DecodeAttnParams:
     """Describe torch tensors: q/out [B, q_len, Hq, D]; k_cache paged
     [P, page_size, Hkv, D] (block_table [B, max_pages] given) or contiguous
-    [B, S, Hkv, D].  Strides are taken from the tensors."""
+    [B, S, Hkv, D].  Strides are taken from the tensors.  A one-byte cache
+    (uint8 or float8_e4m3fn) is an FP8 E4M3 cache with the given scales."""
     B, T, Hq, D = q.shape
     n0, n1, Hkv, D2 = k_cache.shape
     if D2 != D:
@@ -140,6 +145,9 @@ def params_from_tensors(q, k_cache, block_table=None, *, max_seq_len: int,
     p.max_seq_len = int(max_seq_len)
     p.causal = 1 if causal else 0
     p.flags = DA_FLAG_TWO_PASS if two_pass else 0
+    if k_cache.element_size() == 1:
+        p.flags |= DA_FLAG_KV_FP8_E4M3
+    p.k_scale, p.v_scale = float(k_scale), float(v_scale)
     p.scale = float(scale if scale is not None else 1.0 / math.sqrt(D))
     p.q_stride_batch, p.q_stride_token, p.q_stride_head = (int(s) for s in q.stride()[:3])
     o = out if out is not None else q
@@ -189,7 +197,8 @@ def decode_attn_launch_count(p: DecodeAttnParams, num_splits: int) -> int:
 def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
                 causal: bool = False, scale: Optional[float] = None, num_splits: int = 0,
                 out=None, lse=None, workspace=None, status=None, stream=None,
-                params: Optional[DecodeAttnParams] = None, two_pass: bool = False):
+                params: Optional[DecodeAttnParams] = None, two_pass: bool = False,
+                k_scale: float = 1.0, v_scale: float = 1.0):
     """Run decode attention; returns (out bf16 [B, q_len, Hq, D], lse fp32
     [B, q_len, Hq]).  Output, LSE and workspace tensors are allocated with
     torch when not given; `num_splits <= 0` lets the library's planner choose."""
@@ -202,7 +211,7 @@ def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
         lse = torch.empty((B, T, Hq), dtype=torch.float32, device=q.device)
     p = params if params is not None else params_from_tensors(
         q, k_cache, block_table, max_seq_len=max_seq_len, causal=causal, scale=scale, out=out,
-        two_pass=two_pass)
+        two_pass=two_pass, k_scale=k_scale, v_scale=v_scale)
     if num_splits <= 0:
         num_splits, _ = decode_attn_plan(p)
     need = decode_attn_workspace_bytes(p, num_splits)

@@ -79,17 +79,22 @@ int rows_of(const decode_attn_params* p) {
   return (p->num_q_heads / p->num_kv_heads) * p->q_len;
 }
 
+bool kv_fp8(const decode_attn_params* p) { return (p->flags & DA_FLAG_KV_FP8_E4M3) != 0; }
+
 // Shape checks shared by every entry point.
 int check_shape(const decode_attn_params* p) {
   if (p == nullptr) return DA_ERR_NULL_POINTER;
   if (p->batch < 0 || p->batch > 65535 || p->q_len < 1 || p->num_q_heads < 1 ||
       p->num_kv_heads < 1 || p->num_kv_heads > 65535 || p->max_seq_len < 0 ||
-      p->num_q_heads % p->num_kv_heads != 0 || (p->flags & ~DA_FLAG_TWO_PASS) != 0 ||
-      !std::isfinite(p->scale))
+      p->num_q_heads % p->num_kv_heads != 0 ||
+      (p->flags & ~(DA_FLAG_TWO_PASS | DA_FLAG_KV_FP8_E4M3)) != 0 || !std::isfinite(p->scale))
+    return DA_ERR_BAD_SHAPE;
+  if (kv_fp8(p) && (!std::isfinite(p->k_scale) || !std::isfinite(p->v_scale)))
     return DA_ERR_BAD_SHAPE;
   if (p->head_dim != DECODE_ATTN_HEAD_DIM) return DA_ERR_HEAD_DIM;
   if (static_cast<int64_t>(p->num_q_heads / p->num_kv_heads) * p->q_len > DECODE_ATTN_MAX_ROWS)
     return DA_ERR_ROWS;
+  if (kv_fp8(p) && rows_of(p) > dattn::kMaxNarrowRows) return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 
@@ -171,25 +176,36 @@ int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p,
       static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(p->num_kv_heads),
       static_cast<cuuint64_t>(paged ? p->page_size : std::max(p->max_seq_len, 1)),
       static_cast<cuuint64_t>(paged ? p->num_pages : std::max(p->batch, 1))};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p->kv_stride_head) * 2,
-                                 static_cast<cuuint64_t>(p->kv_stride_token) * 2,
-                                 static_cast<cuuint64_t>(p->kv_stride_page) * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kTileTokens), 1};
+  // element bytes: 2 (bf16) or 1 (FP8); a box row is 128 bytes either way
+  // (the 128-byte swizzle span): 64 bf16 (two boxes per 16-token tile) or all
+  // 128 FP8 values of a token (one box)
+  const cuuint64_t eb = kv_fp8(p) ? 1 : 2;
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p->kv_stride_head) * eb,
+                                 static_cast<cuuint64_t>(p->kv_stride_token) * eb,
+                                 static_cast<cuuint64_t>(p->kv_stride_page) * eb};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 1,
+                             static_cast<cuuint32_t>(kTileTokens), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = enc(map, kv_fp8(p) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DA_OK : DA_ERR_ALIGNMENT;
 }
 
 bool stride_ok(int64_t s) { return s > 0 && s % 8 == 0 && s * 2 < (1LL << 40); }
 
+// FP8 caches: strides in bytes, multiples of 16 (the TMA stride rule)
+bool kv_stride_ok(const decode_attn_params* p, int64_t s) {
+  return kv_fp8(p) ? (s > 0 && s % 16 == 0 && s < (1LL << 40)) : stride_ok(s);
+}
+
 // The split pass merges through thread-block clusters (no partials, no
 // combine) when allowed by the flags and when the splits_eff CTAs of every
 // (request, kv head) form a supported cluster and all clusters fit at once.
 bool use_cluster_merge(const decode_attn_params* p, int32_t splits_eff) {
   if ((p->flags & DA_FLAG_TWO_PASS) != 0 || splits_eff < 2 || p->batch < 1) return false;
-  return dattn::split_cluster_merge_fits(rows_of(p), splits_eff,
+  return dattn::split_cluster_merge_fits(rows_of(p), kv_fp8(p), splits_eff,
                                          static_cast<int64_t>(p->batch) * p->num_kv_heads);
 }
 
@@ -224,6 +240,8 @@ void decode_attn_params_init(decode_attn_params* p, int32_t batch, int32_t q_len
   p->kv_stride_token = static_cast<int64_t>(num_kv_heads) * head_dim;
   p->kv_stride_page = p->kv_stride_token * (page_size > 0 ? page_size : max_seq_len);
   p->block_table_stride = max_pages_per_seq;
+  p->k_scale = 1.f;
+  p->v_scale = 1.f;
 }
 
 int decode_attn_plan(const decode_attn_params* p, const int32_t* host_seq_lens,
@@ -300,8 +318,8 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   if (!stride_ok(p->q_stride_batch) || !stride_ok(p->q_stride_token) ||
       !stride_ok(p->q_stride_head) || !stride_ok(p->o_stride_batch) ||
       !stride_ok(p->o_stride_token) || !stride_ok(p->o_stride_head) ||
-      (!no_keys && (!stride_ok(p->kv_stride_page) || !stride_ok(p->kv_stride_token) ||
-                    !stride_ok(p->kv_stride_head))))
+      (!no_keys && (!kv_stride_ok(p, p->kv_stride_page) || !kv_stride_ok(p, p->kv_stride_token) ||
+                    !kv_stride_ok(p, p->kv_stride_head))))
     return DA_ERR_ALIGNMENT;
 
   DeviceInfo di;
@@ -364,7 +382,9 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   a.chunk_len = chunk;
   a.num_splits = eff;
   a.causal = p->causal ? 1 : 0;
-  a.scale_log2 = p->scale * 1.4426950408889634f;
+  a.scale_log2 = p->scale * (kv_fp8(p) ? p->k_scale : 1.f) * 1.4426950408889634f;
+  a.kv_fp8 = kv_fp8(p) ? 1 : 0;
+  a.v_scale = kv_fp8(p) ? p->v_scale : 1.f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dattn::launch_split(kmap, vmap, a, cluster_merge, st) != cudaSuccess) return DA_ERR_CUDA;
@@ -461,6 +481,8 @@ const char* decode_attn_status_string(int code) {
     case DA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case DA_ERR_NO_DEVICE: return "no usable sm_100-class device is current";
     case DA_ERR_SPLITS: return "num_splits / chunk_len out of range";
+    case DA_ERR_UNSUPPORTED:
+      return "FP8 caches run with at most 16 rows per kv head ((Hq/Hkv) * q_len)";
     case DA_ERR_STATIC_WORKSPACE_LIMIT:
       return "the call's partials exceed the 16 MiB static workspace (use fewer splits or decode_attn with a workspace)";
     default: return "unknown status code";

@@ -34,6 +34,8 @@ struct SplitArgs {
   int causal;
   float scale_log2;                    // softmax scale * log2(e)
   int persistent;                      // wide kernel: CTAs walk an item list (set by its launcher)
+  int kv_fp8;                          // caches hold FP8 E4M3 (narrow kernel only)
+  float v_scale;                       // FP8: values = v_scale * V (k_scale is in scale_log2)
 };
 
 struct CombineArgs {
@@ -91,7 +93,7 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
 
 // True when clusters of num_splits CTAs (2..16) are supported and the device
 // can hold num_clusters of them at once (one wave).
-bool split_cluster_merge_fits(int rows, int num_splits, int64_t num_clusters);
+bool split_cluster_merge_fits(int rows, bool fp8, int num_splits, int64_t num_clusters);
 
 // Resident split CTAs per SM for the kernel variant serving `rows` rows.
 int split_ctas_per_sm(int rows);

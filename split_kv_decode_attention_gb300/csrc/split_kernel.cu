@@ -27,6 +27,18 @@
 //     combine kernel (the per-tile LSE buffer of the CUTLASS split-KV post,
 //     §4.2).
 // Exponentials are taken base 2 on scores pre-multiplied by log2(e).
+// FP8 caches (F8): one TMA box carries all 128 E4M3 values of a 16-token tile
+// (half the bytes of bf16), and the MMA operands are built from those bytes in
+// registers (every E4M3 value is an f16 value; cvt.e4m3x2 widens pairs):
+// ldmatrix (b16) on the FP8 K tile gives a thread 4 consecutive d of one key,
+// used as the k pairs (2t4, 2t4+1) and (8+2t4, 9+2t4) of a 16-d step -- a
+// permutation of d inside the step, applied to Q's fragment as well, which
+// leaves the dot product unchanged; ldmatrix.trans (b16) on the FP8 V tile
+// gives a thread 2 d x 2 keys, split by byte permutes into the V^T fragment
+// rows d = 2g4 and 2g4 + 1 of the 16-d output tile (so the O^T accumulator's
+// rows g4 / g4 + 8 are d = 16mt + 2g4 / + 1).  Both products run on f16
+// operands (Q widened from bf16, P rounded to f16); k_scale is folded into the
+// score scale and v_scale into the output.
 // Keys at or past seq_len (and, with the causal mask, past a row's own
 // position) are masked to -inf; V rows past seq_len in a request's last page
 // are zeroed in shared memory first, since those slots may hold anything.
@@ -79,7 +91,7 @@ __device__ __forceinline__ uint32_t load_u32(const uint16_t* p) {
 // thread-block cluster; instead of writing fp32 partials for the combine
 // kernel they merge their results through distributed shared memory and write
 // the final output themselves.
-template <int NT, int STAGES, int TPS, bool CM>
+template <int NT, int STAGES, int TPS, bool CM, bool F8>
 __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
     split_kv_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const SplitArgs a) {
@@ -157,18 +169,31 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
         break;
       }
       const int tiles_here = min(TPS, n_tiles - it * TPS);
-      // page id of the tile this lane loads (lane / 4), picked in registers
+      // page id of the tile this lane loads, picked in registers
+      const int my_tile = F8 ? lane >> 1 : lane >> 2;
       int my_pg = 0;
 #pragma unroll
       for (int i = 0; i < TPS; ++i) {
         const int pg = a.paged ? pw.get(it * TPS + i) : 0;
-        if ((lane >> 2) == i) my_pg = pg;
+        if (my_tile == i) my_pg = pg;
       }
+      constexpr int kBoxBytes = F8 ? C::kTileBytes / 2 : C::kTileBytes;  // K or V of one tile
       if (lane == 0)
-        mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(tiles_here * 2 * C::kTileBytes));
+        mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(tiles_here * 2 * kBoxBytes));
       __syncwarp();
+      if (F8 && lane < tiles_here * 2) {
+        // one TMA box per lane: all 128 FP8 values of 16 tokens (tile =
+        // lane / 2, K or V from lane % 2) into the first half of the tile slot
+        const int i = lane >> 1;
+        const int tok = t_begin + (it * TPS + i) * kTileTokens;
+        const int grp = a.paged ? my_pg : b;
+        const int tin = a.paged ? tok % a.page_size : tok;
+        const bool is_v = (lane & 1) != 0;
+        uint8_t* dst = smem + s * C::kStageBytes + ((is_v ? TPS : 0) + i) * C::kTileBytes;
+        tma_load_4d(dst, is_v ? &v_map : &k_map, &full_bar[s], 0, kvh, tin, grp, policy);
+      }
       // one TMA box per lane (tile = lane / 4; K or V, d-half from lane % 4)
-      if (lane < tiles_here * 4) {
+      if (!F8 && lane < tiles_here * 4) {
         const int i = lane >> 2;
         const int tok = t_begin + (it * TPS + i) * kTileTokens;
         const int grp = a.paged ? my_pg : b;
@@ -218,6 +243,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
       const int d = ks * 16 + 2 * t4;
       qf[ks][nt][0] = qrow ? load_u32(qrow + d) : 0u;
       qf[ks][nt][1] = qrow ? load_u32(qrow + d + 8) : 0u;
+      if constexpr (F8) {  // the d permutation of the FP8 K fragments
+        const int dp = ks * 16 + 4 * t4;
+        qf[ks][nt][0] = qrow ? bf16x2_to_f16x2(load_u32(qrow + dp)) : 0u;
+        qf[ks][nt][1] = qrow ? bf16x2_to_f16x2(load_u32(qrow + dp + 2)) : 0u;
+      }
     }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
@@ -253,19 +283,40 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
       const uint32_t kt = smem_base + s * C::kStageBytes + warp * C::kTileBytes;
       const uint32_t vt = kt + TPS * C::kTileBytes;
       const int tok0 = t_begin + tile * kTileTokens;
-
       // ---- S^T[16 keys x 8*NT rows] = K . Q^T
       float sc[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) sc[nt][i] = 0.f;
+      if constexpr (F8) {
+        // FP8 K tile: 16 rows of 128 bytes, 16-byte chunk c of row t at
+        // (c ^ (t & 7)); one ldmatrix.x4 covers two 16-d steps
+        const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t af[4];
-        ldsm_x4(tile_addr(kt, (lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)), af);
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t r[4];
+          const int chunk = 2 * kp + (lane >> 4);
+          ldsm_x4(kt + key * 128 + ((chunk ^ (key & 7)) << 4), r);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
+          for (int h = 0; h < 2; ++h) {
+            // r[2h]: key g4, d 4t4..4t4+3 of the step; r[2h+1]: key g4 + 8
+            const uint32_t af[4] = {e4m3x2_to_f16x2(r[2 * h]), e4m3x2_to_f16x2(r[2 * h + 1]),
+                                    e4m3x2_to_f16x2(r[2 * h] >> 16),
+                                    e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16_16816(sc[nt], af, qf[2 * kp + h][nt][0], qf[2 * kp + h][nt][1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t af[4];
+          ldsm_x4(tile_addr(kt, (lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)), af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
+        }
       }
 
       // ---- online softmax over this tile (base-2 domain)
@@ -303,8 +354,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
       uint32_t pb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        pb[nt][0] = movmatrix_trans(pack_bf16x2(p[nt][0], p[nt][1]));
-        pb[nt][1] = movmatrix_trans(pack_bf16x2(p[nt][2], p[nt][3]));
+        pb[nt][0] = movmatrix_trans(F8 ? pack_f16x2(p[nt][0], p[nt][1]) : pack_bf16x2(p[nt][0], p[nt][1]));
+        pb[nt][1] = movmatrix_trans(F8 ? pack_f16x2(p[nt][2], p[nt][3]) : pack_bf16x2(p[nt][2], p[nt][3]));
       }
 
       // ---- keys past seq_len: their V slots may hold anything (NaN * 0 is
@@ -312,23 +363,53 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
       if (tok0 + kTileTokens > L) {
         const int first = L - tok0;  // >= 1 since tok0 < t_end <= L
         uint8_t* vgen = smem + s * C::kStageBytes + (TPS + warp) * C::kTileBytes;
-        for (int idx = lane; idx < (kTileTokens - first) * 16; idx += 32) {
-          const int row = first + (idx >> 4);
-          const int c = idx & 15;
-          *reinterpret_cast<uint4*>(vgen + ((c >> 3) << 11) + (row << 7) + ((c & 7) << 4)) =
-              make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (F8) {  // whole 128-byte rows
+          for (int idx = lane; idx < (kTileTokens - first) * 8; idx += 32)
+            *reinterpret_cast<uint4*>(vgen + (first + (idx >> 3)) * 128 + (idx & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          for (int idx = lane; idx < (kTileTokens - first) * 16; idx += 32) {
+            const int row = first + (idx >> 4);
+            const int c = idx & 15;
+            *reinterpret_cast<uint4*>(vgen + ((c >> 3) << 11) + (row << 7) + ((c & 7) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
 
       // ---- O^T[128 d x 8*NT rows] += V^T . P^T
+      if constexpr (F8) {
+        // FP8 V tile, transposed b16 loads: r[i] bytes = (key 2t4: d 2g4,
+        // 2g4+1), (key 2t4+1: d 2g4, 2g4+1) of matrix i; matrices (keys 0-7,
+        // chunk c), (keys 8-15, chunk c), then chunk c + 1
+        const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t af[4];
-        ldsm_x4_trans(tile_addr(vt, (lane & 7) + (lane >> 4) * 8, 2 * mt + ((lane >> 3) & 1)), af);
+        for (int mp = 0; mp < 4; ++mp) {
+          uint32_t r[4];
+          const int chunk = 2 * mp + (lane >> 4);
+          ldsm_x4_trans(vt + key * 128 + ((chunk ^ (key & 7)) << 4), r);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], af, pb[nt][0], pb[nt][1]);
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t af[4] = {
+                e4m3x2_to_f16x2(__byte_perm(r[2 * h], 0, 0x20)),      // d 2g4,     keys 2t4, +1
+                e4m3x2_to_f16x2(__byte_perm(r[2 * h], 0, 0x31)),      // d 2g4 + 1
+                e4m3x2_to_f16x2(__byte_perm(r[2 * h + 1], 0, 0x20)),  // d 2g4,     keys 8 + 2t4, +1
+                e4m3x2_to_f16x2(__byte_perm(r[2 * h + 1], 0, 0x31))}; // d 2g4 + 1
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16_16816(acc[2 * mp + h][nt], af, pb[nt][0], pb[nt][1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t af[4];
+          ldsm_x4_trans(tile_addr(vt, (lane & 7) + (lane >> 4) * 8, 2 * mt + ((lane >> 3) & 1)), af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], af, pb[nt][0], pb[nt][1]);
+        }
       }
     }
     __syncwarp();
@@ -377,12 +458,14 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
 #pragma unroll
       for (int w = 0; w < TPS; ++w)
         Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
-      const float f = Ls > 0.f ? ex2(m[nt][rr] - Mu) / Ls : 0.f;
-      float* dst = red + (warp * C::kRows + row) * C::kRedStride + g4;
+      const float f = (Ls > 0.f ? ex2(m[nt][rr] - Mu) / Ls : 0.f) * (F8 ? a.v_scale : 1.f);
+      // accumulator rows g4 / g4 + 8 of output tile mt hold d = 16mt + g4 /
+      // + 8 (bf16 path) or d = 16mt + 2g4 / + 1 (FP8 path)
+      float* dst = red + (warp * C::kRows + row) * C::kRedStride + (F8 ? 2 * g4 : g4);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         dst[mt * 16] = acc[mt][nt][rr] * f;
-        dst[mt * 16 + 8] = acc[mt][nt][2 + rr] * f;
+        dst[mt * 16 + (F8 ? 1 : 8)] = acc[mt][nt][2 + rr] * f;
       }
     }
   named_barrier_sync(1, 32 * TPS);
@@ -522,21 +605,21 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
 constexpr int kStages = DATTN_STAGES;
 constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
 
-template <int NT, bool CM>
+template <int NT, bool CM, bool F8>
 struct Variant {
   using C = SplitCfg<NT, kStages, kTilesPerStage>;
-  static constexpr auto kernel = split_kv_kernel<NT, kStages, kTilesPerStage, CM>;
+  static constexpr auto kernel = split_kv_kernel<NT, kStages, kTilesPerStage, CM, F8>;
 };
 
 constexpr int kMaxDev = 64;
 constexpr int kMaxCluster = 16;  // non-portable cluster size limit
 std::mutex g_attr_mu;
-bool g_attr_done[2][2][kMaxDev];
-// cached cudaOccupancyMaxActiveClusters per (NT, cluster size, device); -1 unknown
-int g_max_clusters[2][kMaxCluster + 1][kMaxDev];
+bool g_attr_done[2][2][2][kMaxDev];
+// cached cudaOccupancyMaxActiveClusters per (NT, FP8, cluster size, device); -1 unknown
+int g_max_clusters[2][2][kMaxCluster + 1][kMaxDev];
 bool g_max_clusters_init = false;
 
-template <int NT, bool CM>
+template <int NT, bool CM, bool F8>
 cudaError_t ensure_attrs(int* dev_out = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -544,27 +627,28 @@ cudaError_t ensure_attrs(int* dev_out = nullptr) {
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   if (dev_out) *dev_out = dev;
   std::lock_guard<std::mutex> lk(g_attr_mu);
-  if (!g_attr_done[NT - 1][CM][dev]) {
-    e = cudaFuncSetAttribute(Variant<NT, CM>::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Variant<NT, CM>::C::kSmemBytes);
+  if (!g_attr_done[NT - 1][CM][F8][dev]) {
+    e = cudaFuncSetAttribute(Variant<NT, CM, F8>::kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Variant<NT, CM, F8>::C::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (CM) {
-      e = cudaFuncSetAttribute(Variant<NT, CM>::kernel,
+      e = cudaFuncSetAttribute(Variant<NT, CM, F8>::kernel,
                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
     }
-    g_attr_done[NT - 1][CM][dev] = true;
+    g_attr_done[NT - 1][CM][F8][dev] = true;
   }
   return cudaSuccess;
 }
 
-template <int NT, bool CM>
+template <int NT, bool CM, bool F8>
 void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const SplitArgs& a,
                  cudaStream_t st) {
   cfg = {};
   cfg.gridDim = dim3(a.num_splits, a.num_kv_heads, a.batch);
-  cfg.blockDim = dim3(Variant<NT, CM>::C::kThreads);
-  cfg.dynamicSmemBytes = Variant<NT, CM>::C::kSmemBytes;
+  cfg.blockDim = dim3(Variant<NT, CM, F8>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT, CM, F8>::C::kSmemBytes;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -579,24 +663,24 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const 
   }
 }
 
-template <int NT, bool CM>
+template <int NT, bool CM, bool F8>
 cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitArgs& a,
                       cudaStream_t st) {
-  cudaError_t e = ensure_attrs<NT, CM>();
+  cudaError_t e = ensure_attrs<NT, CM, F8>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  fill_config<NT, CM>(cfg, attr, a, st);
-  return cudaLaunchKernelEx(&cfg, Variant<NT, CM>::kernel, km, vm, a);
+  fill_config<NT, CM, F8>(cfg, attr, a, st);
+  return cudaLaunchKernelEx(&cfg, Variant<NT, CM, F8>::kernel, km, vm, a);
 }
 
 template <int NT>
 int ctas_per_sm_nt() {
-  if (ensure_attrs<NT, false>() != cudaSuccess) return 1;
+  if (ensure_attrs<NT, false, false>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Variant<NT, false>::kernel,
-                                                    Variant<NT, false>::C::kThreads,
-                                                    Variant<NT, false>::C::kSmemBytes) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Variant<NT, false, false>::kernel,
+                                                    Variant<NT, false, false>::C::kThreads,
+                                                    Variant<NT, false, false>::C::kSmemBytes) !=
           cudaSuccess ||
       n < 1)
     return 1;
@@ -604,24 +688,25 @@ int ctas_per_sm_nt() {
 }
 
 // How many clusters of `splits` CTAs the device can hold at once.
-template <int NT>
+template <int NT, bool F8>
 int max_active_clusters(int splits) {
   int dev = 0;
-  if (ensure_attrs<NT, true>(&dev) != cudaSuccess) return 0;
+  if (ensure_attrs<NT, true, F8>(&dev) != cudaSuccess) return 0;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (!g_max_clusters_init) {
       for (auto& x : g_max_clusters)
         for (auto& y : x)
-          for (int& z : y) z = -1;
+          for (auto& z : y)
+            for (int& w : z) w = -1;
       g_max_clusters_init = true;
     }
-    if (g_max_clusters[NT - 1][splits][dev] >= 0) return g_max_clusters[NT - 1][splits][dev];
+    if (g_max_clusters[NT - 1][F8][splits][dev] >= 0) return g_max_clusters[NT - 1][F8][splits][dev];
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(splits), 1, 1);
-  cfg.blockDim = dim3(Variant<NT, true>::C::kThreads);
-  cfg.dynamicSmemBytes = Variant<NT, true>::C::kSmemBytes;
+  cfg.blockDim = dim3(Variant<NT, true, F8>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT, true, F8>::C::kSmemBytes;
   cudaLaunchAttribute cl[1];
   cl[0].id = cudaLaunchAttributeClusterDimension;
   cl[0].val.clusterDim.x = static_cast<unsigned>(splits);
@@ -630,12 +715,12 @@ int max_active_clusters(int splits) {
   cfg.attrs = cl;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, Variant<NT, true>::kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, Variant<NT, true, F8>::kernel, &cfg) != cudaSuccess) {
     cudaGetLastError();  // clear the (non-sticky) error of a rejected query
     n = 0;
   }
   std::lock_guard<std::mutex> lk(g_attr_mu);
-  g_max_clusters[NT - 1][splits][dev] = n;
+  g_max_clusters[NT - 1][F8][splits][dev] = n;
   return n;
 }
 
@@ -644,11 +729,18 @@ int max_active_clusters(int splits) {
 cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
                          bool cluster_merge, cudaStream_t stream) {
   if (a.rows > kMaxNarrowRows) return launch_wide(k_map, v_map, a, stream);
+  if (a.kv_fp8) {
+    if (a.rows <= 8)
+      return cluster_merge ? launch_nt<1, true, true>(k_map, v_map, a, stream)
+                           : launch_nt<1, false, true>(k_map, v_map, a, stream);
+    return cluster_merge ? launch_nt<2, true, true>(k_map, v_map, a, stream)
+                         : launch_nt<2, false, true>(k_map, v_map, a, stream);
+  }
   if (a.rows <= 8)
-    return cluster_merge ? launch_nt<1, true>(k_map, v_map, a, stream)
-                         : launch_nt<1, false>(k_map, v_map, a, stream);
-  return cluster_merge ? launch_nt<2, true>(k_map, v_map, a, stream)
-                       : launch_nt<2, false>(k_map, v_map, a, stream);
+    return cluster_merge ? launch_nt<1, true, false>(k_map, v_map, a, stream)
+                         : launch_nt<1, false, false>(k_map, v_map, a, stream);
+  return cluster_merge ? launch_nt<2, true, false>(k_map, v_map, a, stream)
+                       : launch_nt<2, false, false>(k_map, v_map, a, stream);
 }
 
 int split_ctas_per_sm(int rows) {
@@ -656,10 +748,13 @@ int split_ctas_per_sm(int rows) {
   return rows <= 8 ? ctas_per_sm_nt<1>() : ctas_per_sm_nt<2>();
 }
 
-bool split_cluster_merge_fits(int rows, int num_splits, int64_t num_clusters) {
+bool split_cluster_merge_fits(int rows, bool fp8, int num_splits, int64_t num_clusters) {
   if (num_splits < 2 || num_splits > kMaxCluster || num_clusters < 1 || rows > kMaxNarrowRows)
     return false;
-  const int n = rows <= 8 ? max_active_clusters<1>(num_splits) : max_active_clusters<2>(num_splits);
+  const int n = fp8 ? (rows <= 8 ? max_active_clusters<1, true>(num_splits)
+                                 : max_active_clusters<2, true>(num_splits))
+                    : (rows <= 8 ? max_active_clusters<1, false>(num_splits)
+                                 : max_active_clusters<2, false>(num_splits));
   // all clusters resident at once: in multi-wave grids the idle CTAs of short
   // requests hold slots (GB300 sweeps: 1.5-2x slower than partials + combine)
   return n >= num_clusters;

@@ -20,6 +20,13 @@ used for the multi-GB workloads); both round fp32 -> bf16 with
 round-to-nearest-even.  Values are stored as raw bf16 bit patterns (uint16) on
 the host so that no library's bf16 type is involved in the oracle's reading of
 them.
+
+FP8 caches (`kv_fp8` recipes): the same normal K / V values, quantised per
+cache to OCP FP8 E4M3 with one fp32 scale, scale = max|x| / 448 (the largest
+E4M3 value), bytes = E4M3(x / scale) rounded to nearest even by torch's
+float8_e4m3fn conversion -- the cache format with explicit scaling factors
+("Capstone FlashAttention", §2.2 FP8 with scaling; the CUTLASS split-KV post,
+§5.8).  Bytes are stored as uint8.
 """
 from __future__ import annotations
 
@@ -74,6 +81,7 @@ class DecodeShape:
     peaked_key_fraction: float = 0.0   # fraction of K rows multiplied by 8
     head_dim: int = HEAD_DIM
     seed: int = 0
+    kv_fp8: bool = False     # caches in FP8 E4M3 with one scale each
 
     @property
     def group(self) -> int:
@@ -121,6 +129,18 @@ WIDE_WORKLOADS = {
 }
 WORKLOADS.update(WIDE_WORKLOADS)
 
+# FP8 E4M3 caches: the c2 and c5 recipes with the cache quantised per tensor.
+FP8_WORKLOADS = {
+    "f2_b1_mha32_L131072_fp8": DecodeShape(
+        "f2_b1_mha32_L131072_fp8", batch=1, q_len=1, num_q_heads=32, num_kv_heads=32,
+        seq_len_lo=131072, seq_len_hi=131072, paged=False, seed=1008, kv_fp8=True),
+    "f5_b32_q4_causal_h32kv8_L1024-16384_paged_fp8": DecodeShape(
+        "f5_b32_q4_causal_h32kv8_L1024-16384_paged_fp8", batch=32, q_len=4,
+        num_q_heads=32, num_kv_heads=8, seq_len_lo=1024, seq_len_hi=16384,
+        paged=True, causal=True, seed=1009, kv_fp8=True),
+}
+WORKLOADS.update(FP8_WORKLOADS)
+
 
 @dataclasses.dataclass
 class DecodeInputs:
@@ -128,8 +148,8 @@ class DecodeInputs:
 
     Layouts (all row-major, head_dim contiguous):
       q            [B, q_len, Hq, D]                 bf16 bits (uint16) / torch.bfloat16
-      k_cache      paged: [P, page_size, Hkv, D]     same dtype as q
-                   contiguous: [B, max_seq_len, Hkv, D]
+      k_cache      paged: [P, page_size, Hkv, D]     same dtype as q, or E4M3
+                   contiguous: [B, max_seq_len, Hkv, D]   bytes (uint8) with kv_fp8
       v_cache      same as k_cache
       block_table  [B, max_pages_per_seq] int32 (paged; unused slots = -1) or None
       seq_lens     [B] int32 (includes the q_len new tokens)
@@ -144,6 +164,8 @@ class DecodeInputs:
     max_seq_len: int
     num_pages: int           # paged: P; contiguous: 0
     page_size: int           # paged: tokens per page; contiguous: 0
+    k_scale: float = 1.0     # FP8 caches: keys = k_scale * K
+    v_scale: float = 1.0     # FP8 caches: values = v_scale * V
 
     @property
     def kv_strides(self):
@@ -153,10 +175,25 @@ class DecodeInputs:
 
     def kv_bytes(self) -> int:
         """Algorithmic K+V bytes one call must read: every valid token of
-        every request, once per KV head (K row + V row, bf16)."""
+        every request, once per KV head (K row + V row, bf16 or FP8)."""
         lens = np.asarray(_to_numpy_int(self.seq_lens), dtype=np.int64)
         s = self.shape
-        return int(lens.sum()) * s.num_kv_heads * s.head_dim * 2 * 2
+        return int(lens.sum()) * s.num_kv_heads * s.head_dim * 2 * kv_elem_bytes(s)
+
+
+def kv_elem_bytes(shape: DecodeShape) -> int:
+    return 1 if shape.kv_fp8 else 2
+
+
+def quantize_e4m3(x: np.ndarray):
+    """Per-tensor E4M3 quantisation of fp32 values (input preparation):
+    returns (uint8 bytes, fp32 scale) with scale = max|x| / 448."""
+    import torch
+
+    amax = float(np.abs(x).max()) if x.size else 0.0
+    scale = np.float32(amax / 448.0) if amax > 0 else np.float32(1.0)
+    q = torch.from_numpy(np.ascontiguousarray(x / scale, dtype=np.float32))
+    return q.to(torch.float8_e4m3fn).view(torch.uint8).numpy(), float(scale)
 
 
 def _to_numpy_int(x):
@@ -234,6 +271,11 @@ def make_host_inputs(shape: DecodeShape, seed: Optional[int] = None,
     if shape.peaked_key_fraction > 0:
         hit = rng.random(kv_shape[:3]) < shape.peaked_key_fraction
         k[hit] *= np.float32(8.0)   # exact in binary floating point
+    if shape.kv_fp8:
+        kb, ks = quantize_e4m3(k)
+        vb, vs = quantize_e4m3(v)
+        return DecodeInputs(shape, f32_to_bf16_bits(q), kb, vb, bt, seq_lens, max_seq_len,
+                            P, shape.page_size if shape.paged else 0, ks, vs)
     return DecodeInputs(shape, f32_to_bf16_bits(q), f32_to_bf16_bits(k),
                         f32_to_bf16_bits(v), bt, seq_lens, max_seq_len,
                         P, shape.page_size if shape.paged else 0)
@@ -280,10 +322,42 @@ def make_device_inputs(shape: DecodeShape, seed: Optional[int] = None,
             out[i:i + x.shape[0]] = x.to(torch.bfloat16)
         return out
 
+    def normal_e4m3(shp, seed_off, peaked=0.0):
+        # two passes over the same seeded slabs: max|x| for the scale, then
+        # the E4M3 bytes of x / scale (round to nearest even)
+        g2 = torch.Generator(device=device)
+        rows = shp[0]
+        per_row = int(np.prod(shp[1:]))
+        slab = max(1, (1 << 26) // max(1, per_row))
+
+        def slabs():
+            g2.manual_seed(s + seed_off)
+            for i in range(0, rows, slab):
+                x = torch.randn((min(slab, rows - i),) + tuple(shp[1:]), generator=g2,
+                                device=device, dtype=torch.float32)
+                if peaked > 0:
+                    hit = torch.rand(x.shape[:-1], generator=g2, device=device) < peaked
+                    x[hit] *= 8.0
+                yield i, x
+
+        amax = 0.0
+        for _, x in slabs():
+            amax = max(amax, float(x.abs().max()))
+        scale = float(np.float32(amax / 448.0)) if amax > 0 else 1.0
+        out = torch.empty(shp, dtype=torch.uint8, device=device)
+        for i, x in slabs():
+            out[i:i + x.shape[0]] = (x / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        return out, scale
+
     q = normal_bf16((B, T, Hq, D))
+    bt_t = torch.from_numpy(bt).to(device) if bt is not None else None
+    if shape.kv_fp8:
+        k, ks = normal_e4m3(kv_shape, 101, shape.peaked_key_fraction)
+        v, vs = normal_e4m3(kv_shape, 202)
+        return DecodeInputs(shape, q, k, v, bt_t, torch.from_numpy(seq_lens).to(device),
+                            max_seq_len, P, shape.page_size if shape.paged else 0, ks, vs)
     k = normal_bf16(kv_shape, shape.peaked_key_fraction)
     v = normal_bf16(kv_shape)
-    bt_t = torch.from_numpy(bt).to(device) if bt is not None else None
     return DecodeInputs(shape, q, k, v, bt_t, torch.from_numpy(seq_lens).to(device),
                         max_seq_len, P, shape.page_size if shape.paged else 0)
 
@@ -291,10 +365,11 @@ def make_device_inputs(shape: DecodeShape, seed: Optional[int] = None,
 def small_shape(name: str = "small", batch: int = 3, q_len: int = 1,
                 num_q_heads: int = 8, num_kv_heads: int = 2, lo: int = 1,
                 hi: int = 300, paged: bool = True, page_size: int = 16,
-                causal: bool = False, peaked: float = 0.0, seed: int = 7) -> DecodeShape:
+                causal: bool = False, peaked: float = 0.0, seed: int = 7,
+                kv_fp8: bool = False) -> DecodeShape:
     """A small workload of the same structure, for tests the oracle finishes
     in well under a second."""
     return DecodeShape(name, batch=batch, q_len=q_len, num_q_heads=num_q_heads,
                        num_kv_heads=num_kv_heads, seq_len_lo=lo, seq_len_hi=hi,
                        paged=paged, page_size=page_size, causal=causal,
-                       peaked_key_fraction=peaked, seed=seed)
+                       peaked_key_fraction=peaked, seed=seed, kv_fp8=kv_fp8)

@@ -56,15 +56,21 @@ def assert_lse_close(got, ref, what="lse"):
 
 
 def to_device(inp, device="cuda"):
-    """Upload a host DecodeInputs (numpy bf16 bits) to torch device tensors."""
+    """Upload a host DecodeInputs (numpy bf16 bits, FP8 caches as bytes) to
+    torch device tensors."""
     import torch
 
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
             torch.bfloat16).to(device)
 
+    def kv(a):  # bf16 bits, or FP8 E4M3 bytes as uint8
+        if a.dtype == np.uint8:
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+        return bf(a)
+
     bt = None if inp.block_table is None else torch.from_numpy(inp.block_table).to(device)
-    return (bf(inp.q), bf(inp.k_cache), bf(inp.v_cache), bt,
+    return (bf(inp.q), kv(inp.k_cache), kv(inp.v_cache), bt,
             torch.from_numpy(np.ascontiguousarray(inp.seq_lens)).to(device))
 
 

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_params_struct_layout_matches_header(lib):
-    assert ctypes.sizeof(binding.DecodeAttnParams) == 128
+    assert ctypes.sizeof(binding.DecodeAttnParams) == 136
     p = binding.decode_attn_params_init(4, 2, 32, 8, 128, 16, 10, 100, 160, True)
     assert (p.batch, p.q_len, p.num_q_heads, p.num_kv_heads, p.head_dim) == (4, 2, 32, 8, 128)
     assert (p.page_size, p.max_pages_per_seq, p.num_pages, p.max_seq_len, p.causal) == \
@@ -52,6 +52,7 @@ def test_params_struct_layout_matches_header(lib):
     assert (p.q_stride_batch, p.q_stride_token, p.q_stride_head) == (2 * 32 * 128, 32 * 128, 128)
     assert (p.kv_stride_page, p.kv_stride_token, p.kv_stride_head) == (16 * 8 * 128, 8 * 128, 128)
     assert p.block_table_stride == 10
+    assert (p.k_scale, p.v_scale, p.flags) == (1.0, 1.0, 0)
 
 
 def _call(lib, p, **kw):
@@ -65,7 +66,7 @@ def _call(lib, p, **kw):
 
 @pytest.mark.parametrize("field,value,code", [
     ("head_dim", 64, -3), ("num_kv_heads", 3, -2), ("q_len", 0, -2), ("batch", -1, -2),
-    ("max_seq_len", -5, -2), ("flags", 2, -2)])
+    ("max_seq_len", -5, -2), ("flags", 4, -2)])
 def test_shape_errors_are_reported_before_launch(lib, field, value, code):
     p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 0, 0, 0, 64, False)
     setattr(p, field, value)
@@ -86,6 +87,25 @@ def test_null_and_alignment_errors(lib):
     assert _call(lib, p, k=24) == -6           # k base not 16-byte aligned
     p.kv_stride_token = 100                     # not a multiple of 8 elements
     assert _call(lib, p) == -6
+
+
+def test_fp8_cache_argument_errors(lib):
+    """FP8 E4M3 caches: byte strides must be multiples of 16, the scales finite,
+    and at most 16 rows per kv head run (the tcgen05 kernel reads bf16 only)."""
+    p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 0, 0, 0, 64, False)
+    p.flags = binding.DA_FLAG_KV_FP8_E4M3
+    p.kv_stride_token = 2 * 128 + 8               # a multiple of 8 but not of 16 bytes
+    assert _call(lib, p) == -6
+    p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 0, 0, 0, 64, False)
+    p.flags = binding.DA_FLAG_KV_FP8_E4M3
+    p.k_scale = float("inf")
+    assert _call(lib, p) == -2
+    p = binding.decode_attn_params_init(1, 4, 64, 8, 128, 0, 0, 0, 64, True)  # 8 x 4 = 32 rows
+    p.flags = binding.DA_FLAG_KV_FP8_E4M3
+    assert _call(lib, p) == binding.DA_ERR_UNSUPPORTED
+    assert "16 rows" in binding.decode_attn_status_string(binding.DA_ERR_UNSUPPORTED)
+    p.flags = 0                                   # the same shape with bf16 caches is fine
+    assert _call(lib, p) != binding.DA_ERR_UNSUPPORTED
 
 
 def test_paging_errors(lib):

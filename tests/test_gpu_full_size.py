@@ -1,4 +1,4 @@
-"""Full-size parity on the five decode workloads, in the launch configuration
+"""Full-size parity on the decode workloads (bf16 and FP8 caches), in the launch configuration
 the benchmark times (the library planner fed the host sequence lengths).
 
 The oracle computes a sample of output rows one by one (every row of a few
@@ -29,17 +29,20 @@ def binding():
 
 
 def host_bits(t):
+    if t.element_size() == 1:   # FP8 E4M3 bytes
+        return t.contiguous().cpu().numpy().view(np.uint8)
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("name", W.WORKLOAD_ORDER + list(W.WIDE_WORKLOADS))
+@pytest.mark.parametrize("name", W.WORKLOAD_ORDER + list(W.WIDE_WORKLOADS) + list(W.FP8_WORKLOADS))
 def test_full_size_workload_sampled_rows_match_oracle(binding, name):
     shape = W.WORKLOADS[name]
     inp = W.make_device_inputs(shape, device="cuda")
     lens_h = inp.seq_lens.cpu().numpy()
     q, k, v, bt, lens = inp.q, inp.k_cache, inp.v_cache, inp.block_table, inp.seq_lens
     p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len,
-                                    causal=shape.causal, scale=shape.scale)
+                                    causal=shape.causal, scale=shape.scale,
+                                    k_scale=inp.k_scale, v_scale=inp.v_scale)
     S, _ = binding.decode_attn_plan(p, lens_h)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len,
@@ -50,7 +53,7 @@ def test_full_size_workload_sampled_rows_match_oracle(binding, name):
 
     o = bf16_tensor_to_f64(out)
     l = lse.cpu().numpy()
-    vmax = float(v.float().abs().max().item())
+    vmax = 448.0 * inp.v_scale if shape.kv_fp8 else float(v.float().abs().max().item())
     assert np.all(np.isfinite(o))
     assert np.abs(o).max() <= vmax + 1e-2
     assert np.all(np.isfinite(l[lens_h > 0]))
@@ -64,7 +67,8 @@ def test_full_size_workload_sampled_rows_match_oracle(binding, name):
     rows = np.array(sorted(set(rows)), np.int32)
     host = W.DecodeInputs(shape, host_bits(q), host_bits(k), host_bits(v),
                           None if bt is None else bt.cpu().numpy(), lens_h,
-                          inp.max_seq_len, inp.num_pages, inp.page_size)
+                          inp.max_seq_len, inp.num_pages, inp.page_size, inp.k_scale,
+                          inp.v_scale)
     ref_o, ref_l = oracle.decode_attention_inputs(host, rows=rows)
     assert_out_close(o.reshape(-1, 128)[rows], ref_o, what=name)
     assert_lse_close(l.reshape(-1)[rows], ref_l, what=name)

@@ -29,6 +29,32 @@ def bf(a):
 
 
 # ---------------------------------------------------------------- paging
+@pytest.mark.parametrize("splits", [1, 3])
+def test_fp8_shuffled_pages_bit_identical_to_contiguous(binding, splits):
+    """FP8 E4M3 caches: the same logical bytes contiguous and as shuffled
+    pages give identical bits out."""
+    rng = np.random.default_rng(60 + splits)
+    B, Lmax, Hkv, Hq, D = 5, 1000, 2, 8, 128
+    kc, ks = W.quantize_e4m3(rng.standard_normal((B, Lmax, Hkv, D), dtype=np.float32))
+    vc, vs = W.quantize_e4m3(rng.standard_normal((B, Lmax, Hkv, D), dtype=np.float32))
+    q = W.f32_to_bf16_bits(rng.standard_normal((B, 1, Hq, D), dtype=np.float32))
+    lens = np.array([1000, 1, 333, 16, 777], np.int32)
+    kp, vp, bt = paginate(kc, vc, lens, 16, rng)
+    lens_d = torch.from_numpy(lens).cuda()
+    u8 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    o1, l1 = binding.decode_attn(bf(q), u8(kc), u8(vc), None, lens_d, max_seq_len=Lmax,
+                                 num_splits=splits, k_scale=ks, v_scale=vs)
+    o2, l2 = binding.decode_attn(bf(q), u8(kp), u8(vp), torch.from_numpy(bt).cuda(), lens_d,
+                                 max_seq_len=Lmax, num_splits=splits, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_tensor_to_bits(o1), bf16_tensor_to_bits(o2))
+    assert np.array_equal(l1.cpu().numpy().view(np.uint32), l2.cpu().numpy().view(np.uint32))
+    ref_o, ref_l = oracle.decode_attention(q, kc, vc, lens, num_kv_heads=Hkv, kv_fp8=True,
+                                           k_scale=ks, v_scale=vs)
+    assert_out_close(bf16_tensor_to_f64(o2), ref_o)
+    assert_lse_close(l2.cpu().numpy(), ref_l)
+
+
 @pytest.mark.parametrize("page_size", [16, 32, 128])
 @pytest.mark.parametrize("splits", [1, 3])
 def test_shuffled_pages_bit_identical_to_contiguous(binding, page_size, splits):

@@ -31,7 +31,8 @@ def run(binding, inp, num_splits=0, status=None, **kw):
     q, k, v, bt, lens = to_device(inp)
     out, lse = binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len,
                                    causal=inp.shape.causal, scale=inp.shape.scale,
-                                   num_splits=num_splits, status=status, **kw)
+                                   num_splits=num_splits, status=status,
+                                   k_scale=inp.k_scale, v_scale=inp.v_scale, **kw)
     torch.cuda.synchronize()
     return out, lse
 
@@ -185,3 +186,41 @@ def test_wide_schedule_batch_sizes(binding, batch):
     for S in (1, 3):
         out, lse = check(binding, inp, S)
         assert np.all(bf16_tensor_to_f64(out)[lens == 0] == 0)
+
+
+
+# FP8 E4M3 caches (one scale per cache): the narrow kernel widens them to f16
+FP8_CASES = [
+    # name, G, q_len, causal, paged, page_size, lo, hi
+    ("f8_mha_contig", 1, 1, False, False, 16, 1, 700),
+    ("f8_gqa4_paged", 4, 1, False, True, 16, 1, 900),
+    ("f8_gqa8_paged_peaked", 8, 1, False, True, 16, 100, 1200),
+    ("f8_gqa4_q4_causal", 4, 4, True, True, 16, 4, 800),
+    ("f8_gqa16_paged", 16, 1, False, True, 16, 1, 400),
+    ("f8_mha_q16_causal", 1, 16, True, True, 16, 16, 300),
+    ("f8_gqa4_q2_page32", 4, 2, True, True, 32, 2, 700),
+]
+
+
+@pytest.mark.parametrize("two_pass", [False, True], ids=["merge-auto", "two-pass"])
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+@pytest.mark.parametrize("case", FP8_CASES, ids=[c[0] for c in FP8_CASES])
+def test_fp8_cache_workloads_match_oracle(binding, case, splits, two_pass):
+    name, G, T, causal, paged, ps, lo, hi = case
+    shp = W.small_shape(name, batch=4, q_len=T, num_q_heads=2 * G, num_kv_heads=2,
+                        lo=lo, hi=hi, paged=paged, page_size=ps, causal=causal,
+                        peaked=0.05 if "peaked" in name else 0.0, seed=200 + G + T,
+                        kv_fp8=True)
+    inp = W.make_host_inputs(shp)
+    check(binding, inp, splits, two_pass)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_fp8_edge_lengths_including_empty_requests(binding, splits):
+    lens = np.array([0, 1, 15, 16, 17, 63, 64, 65, 127, 129, 0, 250], np.int32)
+    shp = W.small_shape("f8_edges", batch=len(lens), num_q_heads=8, num_kv_heads=2,
+                        lo=0, hi=256, paged=True, seed=37, kv_fp8=True)
+    inp = W.make_host_inputs(shp, seq_lens=lens)
+    out, lse = check(binding, inp, splits)
+    assert np.all(bf16_tensor_to_f64(out)[[0, 10]] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[[0, 10]]))

@@ -228,7 +228,7 @@ def paginate(kc, vc, seq_lens, page_size, rng):
     need = [(int(L) + page_size - 1) // page_size for L in seq_lens]
     P = sum(need)
     perm = rng.permutation(P)
-    kp = np.zeros((P, page_size, Hkv, D), np.uint16)
+    kp = np.zeros((P, page_size, Hkv, D), kc.dtype)
     vp = np.zeros_like(kp)
     bt = np.full((B, max(need)), -1, np.int32)
     off = 0
@@ -408,3 +408,86 @@ def test_tiled_online_recurrence_within_pages_error_bound():
         m = m_new
     tiled = acc / l[:, None]
     assert np.abs(tiled - ref).max() < 1e-10
+
+
+# ---------------------------------------------------------------- FP8 E4M3 caches
+def test_e4m3_decoding_matches_torch_float8_for_every_code():
+    """The oracle's E4M3 decoder (written from the format definition) against
+    PyTorch's float8_e4m3fn for all 256 codes; NaN exactly at S.1111.111."""
+    torch = pytest.importorskip("torch")
+    mine = oracle.e4m3_values()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))   # -0 is 0x80
+
+
+def test_e4m3_closed_forms():
+    v = oracle.e4m3_values()
+    assert v[0x38] == 1.0 and v[0xB8] == -1.0          # exponent field 7 = bias
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0      # largest finite value
+    assert v[0x08] == 2.0 ** -6                        # smallest normal
+    assert v[0x01] == 2.0 ** -9                        # smallest subnormal
+    assert v[0x07] == 7 * 2.0 ** -9                    # largest subnormal
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert v[0x00] == 0.0 and np.signbit(v[0x80])
+
+
+def _fp8_problem(seed, k_scale, v_scale, paged=True, causal=True):
+    shp = W.small_shape("f8pin", batch=3, q_len=2, num_q_heads=8, num_kv_heads=2,
+                        lo=3, hi=70, paged=paged, causal=causal, seed=seed, kv_fp8=True)
+    inp = W.make_host_inputs(shp)
+    inp.k_scale, inp.v_scale = k_scale, v_scale
+    return inp
+
+
+@pytest.mark.parametrize("paged", [True, False])
+def test_fp8_cache_equals_bf16_cache_of_the_decoded_values(paged):
+    """With power-of-two scales every k_scale * E4M3 value is a bf16 value, so
+    the FP8 path must give exactly the bf16 path on those values."""
+    inp = _fp8_problem(50, 2.0 ** -3, 2.0 ** 2, paged=paged)
+    vals = oracle.e4m3_values()
+    kb = bf16(vals[inp.k_cache] * inp.k_scale)
+    vb = bf16(vals[inp.v_cache] * inp.v_scale)
+    assert np.array_equal(f32(kb).astype(np.float64), vals[inp.k_cache] * inp.k_scale)
+    o8, l8 = oracle.decode_attention_inputs(inp)
+    s = inp.shape
+    o16, l16 = oracle.decode_attention(
+        inp.q, kb, vb, inp.seq_lens, num_kv_heads=s.num_kv_heads,
+        block_table=inp.block_table, page_size=inp.page_size, num_pages=inp.num_pages,
+        scale=s.scale, causal=s.causal)
+    assert np.array_equal(o8, o16) and np.array_equal(l8, l16)
+
+
+def test_fp8_value_scale_is_linear_and_key_scale_scales_the_scores():
+    inp = _fp8_problem(51, 0.01, 0.02)
+    o1, l1 = oracle.decode_attention_inputs(inp)
+    inp.v_scale = 0.04                       # doubling v_scale doubles the output
+    o2, l2 = oracle.decode_attention_inputs(inp)
+    np.testing.assert_allclose(o2, 2 * o1, rtol=1e-14, atol=1e-300)
+    assert np.array_equal(l1, l2)
+    # k_scale enters only as a factor on the scores: k_scale * c with softmax
+    # scale s equals k_scale c' = k_scale * c / 2 with softmax scale 2 s
+    s = inp.shape
+    o3, l3 = oracle.decode_attention(
+        inp.q, inp.k_cache, inp.v_cache, inp.seq_lens, num_kv_heads=s.num_kv_heads,
+        block_table=inp.block_table, page_size=inp.page_size, num_pages=inp.num_pages,
+        scale=2 * s.scale, causal=s.causal, kv_fp8=True, k_scale=0.005, v_scale=0.04)
+    np.testing.assert_allclose(o3, o2, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l3, l2, rtol=1e-12, atol=1e-14)
+
+
+def test_fp8_workload_recipe_quantises_within_half_an_e4m3_step():
+    """Input-recipe check: every stored byte decodes to within half an E4M3
+    step of x / scale (round to nearest), and the largest |x| maps to 448."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((64, 128)).astype(np.float32)
+    b, sc = W.quantize_e4m3(x)
+    vals = oracle.e4m3_values()[b]
+    y = x.astype(np.float64) / sc
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6))) - 3)
+    assert np.all(np.abs(vals - y) <= ulp / 2 + 1e-12)
+    assert np.abs(vals).max() == 448.0
