@@ -129,7 +129,7 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
   const int rows = rows_of(p);
   const int64_t max_tiles = ceil_div64(std::max(p->max_seq_len, 1), kTileTokens);
   const int64_t pairs = static_cast<int64_t>(std::max(p->batch, 1)) * p->num_kv_heads;
-  const int64_t slots = static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows);
+  const int64_t slots = static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows, kv_fp8(p));
   bool uniform = true;
   int64_t work_tokens = 0;
   if (host_seq_lens != nullptr) {

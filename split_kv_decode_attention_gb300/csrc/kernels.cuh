@@ -96,7 +96,7 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
 bool split_cluster_merge_fits(int rows, bool fp8, int num_splits, int64_t num_clusters);
 
 // Resident split CTAs per SM for the kernel variant serving `rows` rows.
-int split_ctas_per_sm(int rows);
+int split_ctas_per_sm(int rows, bool fp8);
 
 // Launch the tcgen05 kernel for 17..128 rows per kv head (same grid, same
 // outputs and partials as launch_split without cluster merge).

@@ -55,11 +55,12 @@ namespace {
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int NT, int STAGES, int TPS>
+template <int NT, int STAGES, int TPS, bool F8 = false>
 struct SplitCfg {
   static constexpr int kThreads = 32 * (TPS + 1);        // TPS consumer warps + 1 producer
   static constexpr int kHalfBytes = kTileTokens * 64 * 2;  // [16 tokens][64 d] bf16
-  static constexpr int kTileBytes = 2 * kHalfBytes;        // one 16-token K (or V) tile
+  // one 16-token K (or V) tile: two bf16 halves, or 16 rows of 128 FP8 bytes
+  static constexpr int kTileBytes = F8 ? kTileTokens * 128 : 2 * kHalfBytes;
   static constexpr int kStageBytes = 2 * TPS * kTileBytes;  // TPS K tiles, then TPS V tiles
   static constexpr int kPipeBytes = STAGES * kStageBytes;
   static constexpr int kRows = 8 * NT;                     // padded query rows
@@ -92,10 +93,10 @@ __device__ __forceinline__ uint32_t load_u32(const uint16_t* p) {
 // kernel they merge their results through distributed shared memory and write
 // the final output themselves.
 template <int NT, int STAGES, int TPS, bool CM, bool F8>
-__global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
+__global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     split_kv_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const SplitArgs a) {
-  using C = SplitCfg<NT, STAGES, TPS>;
+  using C = SplitCfg<NT, STAGES, TPS, F8>;
   constexpr uint32_t kFull = 0xffffffffu;
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
         const int pg = a.paged ? pw.get(it * TPS + i) : 0;
         if (my_tile == i) my_pg = pg;
       }
-      constexpr int kBoxBytes = F8 ? C::kTileBytes / 2 : C::kTileBytes;  // K or V of one tile
+      constexpr int kBoxBytes = C::kTileBytes;  // K or V of one tile
       if (lane == 0)
         mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(tiles_here * 2 * kBoxBytes));
       __syncwarp();
@@ -604,11 +605,22 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS>::kThreads)
 #endif
 constexpr int kStages = DATTN_STAGES;
 constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
+// FP8 caches: tiles are half the bytes, so the same ring holds more stages
+#ifndef DATTN_F8_STAGES
+#define DATTN_F8_STAGES 6
+#endif
+#ifndef DATTN_F8_TILES_PER_STAGE
+#define DATTN_F8_TILES_PER_STAGE 2
+#endif
+constexpr int kF8Stages = DATTN_F8_STAGES;
+constexpr int kF8TilesPerStage = DATTN_F8_TILES_PER_STAGE;
 
 template <int NT, bool CM, bool F8>
 struct Variant {
-  using C = SplitCfg<NT, kStages, kTilesPerStage>;
-  static constexpr auto kernel = split_kv_kernel<NT, kStages, kTilesPerStage, CM, F8>;
+  static constexpr int kSt = F8 ? kF8Stages : kStages;
+  static constexpr int kTps = F8 ? kF8TilesPerStage : kTilesPerStage;
+  using C = SplitCfg<NT, kSt, kTps, F8>;
+  static constexpr auto kernel = split_kv_kernel<NT, kSt, kTps, CM, F8>;
 };
 
 constexpr int kMaxDev = 64;
@@ -674,13 +686,13 @@ cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitA
   return cudaLaunchKernelEx(&cfg, Variant<NT, CM, F8>::kernel, km, vm, a);
 }
 
-template <int NT>
+template <int NT, bool F8>
 int ctas_per_sm_nt() {
-  if (ensure_attrs<NT, false, false>() != cudaSuccess) return 1;
+  if (ensure_attrs<NT, false, F8>() != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Variant<NT, false, false>::kernel,
-                                                    Variant<NT, false, false>::C::kThreads,
-                                                    Variant<NT, false, false>::C::kSmemBytes) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Variant<NT, false, F8>::kernel,
+                                                    Variant<NT, false, F8>::C::kThreads,
+                                                    Variant<NT, false, F8>::C::kSmemBytes) !=
           cudaSuccess ||
       n < 1)
     return 1;
@@ -743,9 +755,10 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
                        : launch_nt<2, false, false>(k_map, v_map, a, stream);
 }
 
-int split_ctas_per_sm(int rows) {
+int split_ctas_per_sm(int rows, bool fp8) {
   if (rows > kMaxNarrowRows) return wide_ctas_per_sm();
-  return rows <= 8 ? ctas_per_sm_nt<1>() : ctas_per_sm_nt<2>();
+  if (fp8) return rows <= 8 ? ctas_per_sm_nt<1, true>() : ctas_per_sm_nt<2, true>();
+  return rows <= 8 ? ctas_per_sm_nt<1, false>() : ctas_per_sm_nt<2, false>();
 }
 
 bool split_cluster_merge_fits(int rows, bool fp8, int num_splits, int64_t num_clusters) {
