@@ -121,9 +121,16 @@ static int64_t kv_row(const oracle_job *J, int b, int64_t j, int kvh, int *err) 
   return page * J->stride_page + slot * J->stride_tok + (int64_t)kvh * J->stride_head;
 }
 
+/* e4m3_to_double of every code, filled once (the same definition, looked up). */
+static double g_e4m3[256];
+static pthread_once_t g_e4m3_once = PTHREAD_ONCE_INIT;
+static void fill_e4m3(void) {
+  for (int c = 0; c < 256; ++c) g_e4m3[c] = e4m3_to_double((uint8_t)c);
+}
+
 /* Element `e` of a cache as a real number. */
 static double kv_value(const oracle_job *J, const void *base, double scale, int64_t e) {
-  if (J->kv_fp8) return scale * e4m3_to_double(((const uint8_t *)base)[e]);
+  if (J->kv_fp8) return scale * g_e4m3[((const uint8_t *)base)[e]];
   return bf16_to_double(((const uint16_t *)base)[e]);
 }
 
@@ -227,6 +234,7 @@ int oracle_decode_attn(int batch, int q_len, int num_q_heads, int num_kv_heads,
   J.num_kv_heads = num_kv_heads; J.head_dim = head_dim;
   J.q = q; J.k = k; J.v = v;
   J.kv_fp8 = kv_fp8; J.k_scale = k_scale; J.v_scale = v_scale;
+  if (kv_fp8) pthread_once(&g_e4m3_once, fill_e4m3);
   J.stride_page = stride_page; J.stride_tok = stride_tok; J.stride_head = stride_head;
   J.page_size = page_size; J.block_table = block_table; J.bt_stride = bt_stride;
   J.max_pages_per_seq = max_pages_per_seq; J.num_pages = num_pages;

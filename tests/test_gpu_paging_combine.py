@@ -246,3 +246,41 @@ def test_call_replays_inside_a_cuda_graph(binding):
     ref_o, ref_l = oracle.decode_attention_inputs(inp)
     assert_out_close(bf16_tensor_to_f64(out), ref_o)
     assert_lse_close(lse.cpu().numpy(), ref_l)
+
+
+
+@pytest.mark.parametrize("kind", ["wide", "fp8"])
+def test_wide_and_fp8_calls_replay_inside_a_cuda_graph(binding, kind):
+    """The persistent tcgen05 kernel (64 rows per KV head) and the FP8-cache
+    path captured in a CUDA graph and replayed."""
+    if kind == "wide":
+        shp = W.small_shape("graph_w", batch=5, q_len=8, num_q_heads=16, num_kv_heads=2,
+                            lo=100, hi=3000, causal=True, seed=49)
+    else:
+        shp = W.small_shape("graph_f8", batch=4, q_len=2, num_q_heads=8, num_kv_heads=2,
+                            lo=100, hi=3000, causal=True, seed=50, kv_fp8=True)
+    inp = W.make_host_inputs(shp)
+    q, k, v, bt, lens = to_device(inp)
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True,
+                                    k_scale=inp.k_scale, v_scale=inp.v_scale)
+    S = 3
+    ws = torch.empty((binding.decode_attn_workspace_bytes(p, S) + 3) // 4 + 1,
+                     dtype=torch.float32, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len, num_splits=S,
+                            out=out, lse=lse, workspace=ws, params=p, stream=s)   # warm-up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len, num_splits=S,
+                            out=out, lse=lse, workspace=ws, params=p, stream=s)
+    out.zero_()
+    lse.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.decode_attention_inputs(inp)
+    assert_out_close(bf16_tensor_to_f64(out), ref_o)
+    assert_lse_close(lse.cpu().numpy(), ref_l)

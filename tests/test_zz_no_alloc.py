@@ -36,7 +36,7 @@ def both_ways(binding, inp, num_splits):
     q, k, v, bt, lens = to_device(inp)
     s = inp.shape
     p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=s.causal,
-                                    scale=s.scale)
+                                    scale=s.scale, k_scale=inp.k_scale, v_scale=inp.v_scale)
     ref_out, ref_lse = binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len,
                                            causal=s.causal, scale=s.scale,
                                            num_splits=num_splits, params=p)
@@ -59,6 +59,21 @@ def test_two_calls_in_a_row_match_decode_attn(binding):
         "na2", batch=2, q_len=1, num_q_heads=8, num_kv_heads=8, lo=9000, hi=12000,
         paged=False, seed=92))
     for inp, splits in ((first, 6), (second, 0)):
+        out, lse, ref_out, ref_lse = both_ways(binding, inp, splits)
+        assert_out_close(out, ref_out, what="static-workspace out")
+        assert_lse_close(lse, ref_lse, what="static-workspace lse")
+
+
+def test_fp8_and_wide_calls_match_decode_attn(binding):
+    """FP8 caches and a 64-row query group (the tcgen05 kernel) through the
+    static workspace."""
+    f8 = W.make_host_inputs(W.small_shape(
+        "na3", batch=4, q_len=2, num_q_heads=8, num_kv_heads=2, lo=30, hi=2500,
+        paged=True, causal=True, seed=93, kv_fp8=True))
+    wide = W.make_host_inputs(W.small_shape(
+        "na4", batch=3, q_len=8, num_q_heads=16, num_kv_heads=2, lo=30, hi=2500,
+        paged=True, causal=True, seed=94))
+    for inp, splits in ((f8, 5), (wide, 4)):
         out, lse, ref_out, ref_lse = both_ways(binding, inp, splits)
         assert_out_close(out, ref_out, what="static-workspace out")
         assert_lse_close(lse, ref_lse, what="static-workspace lse")
