@@ -26,6 +26,7 @@ DA_STATUS_SHORT_CAUSAL = 4
 DA_STATUS_TIMEOUT = 8
 DA_FLAG_TWO_PASS = 1
 DA_FLAG_KV_FP8_E4M3 = 2
+DA_FLAG_TEST_WITHHOLD_COPY = 0x100
 DA_ERR_UNSUPPORTED = -12
 
 EXPORTED_SYMBOLS = (

@@ -87,7 +87,8 @@ int check_shape(const decode_attn_params* p) {
   if (p->batch < 0 || p->batch > 65535 || p->q_len < 1 || p->num_q_heads < 1 ||
       p->num_kv_heads < 1 || p->num_kv_heads > 65535 || p->max_seq_len < 0 ||
       p->num_q_heads % p->num_kv_heads != 0 ||
-      (p->flags & ~(DA_FLAG_TWO_PASS | DA_FLAG_KV_FP8_E4M3)) != 0 || !std::isfinite(p->scale))
+      (p->flags & ~(DA_FLAG_TWO_PASS | DA_FLAG_KV_FP8_E4M3 | DA_FLAG_TEST_WITHHOLD_COPY)) != 0 ||
+      !std::isfinite(p->scale))
     return DA_ERR_BAD_SHAPE;
   if (kv_fp8(p) && (!std::isfinite(p->k_scale) || !std::isfinite(p->v_scale)))
     return DA_ERR_BAD_SHAPE;
@@ -384,6 +385,7 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   a.causal = p->causal ? 1 : 0;
   a.scale_log2 = p->scale * (kv_fp8(p) ? p->k_scale : 1.f) * 1.4426950408889634f;
   a.kv_fp8 = kv_fp8(p) ? 1 : 0;
+  a.test_withhold = (p->flags & DA_FLAG_TEST_WITHHOLD_COPY) != 0 ? 1 : 0;
   a.v_scale = kv_fp8(p) ? p->v_scale : 1.f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -36,6 +36,7 @@ struct SplitArgs {
   int persistent;                      // wide kernel: CTAs walk an item list (set by its launcher)
   int kv_fp8;                          // caches hold FP8 E4M3 (narrow kernel only)
   float v_scale;                       // FP8: values = v_scale * V (k_scale is in scale_log2)
+  int test_withhold;                   // DA_FLAG_TEST_WITHHOLD_COPY (narrow kernel, two-pass)
 };
 
 struct CombineArgs {

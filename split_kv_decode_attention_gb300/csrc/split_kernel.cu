@@ -159,6 +159,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     if (a.paged) pw.init();
     int issued = 0;
     bool ok = true;
+    const bool withhold =
+        a.test_withhold != 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
     for (int it = 0; it < n_iters; ++it) {
       const int s = it % STAGES;
       const int use = it / STAGES;
@@ -179,6 +181,13 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         if (my_tile == i) my_pg = pg;
       }
       constexpr int kBoxBytes = C::kTileBytes;  // K or V of one tile
+      // test hook (DA_FLAG_TEST_WITHHOLD_COPY): block (0, 0, 0) of a two-pass
+      // launch never fills its first stage, so its consumers' bounded wait
+      // runs out and reports DA_STATUS_TIMEOUT
+      if (!CM && it == 0 && withhold) {
+        ++issued;
+        continue;
+      }
       if (lane == 0)
         mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(tiles_here * 2 * kBoxBytes));
       __syncwarp();
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
       // do not leave while copies are in flight: wait (bounded) for the last
       // stages this warp issued
       for (int it = max(0, issued - STAGES); it < issued; ++it)
-        mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1);
+        if (!(withhold && it == 0)) mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1);
     }
     if constexpr (CM) {
       // the consumers' two cluster barriers need every thread of the cluster

@@ -108,6 +108,12 @@ def test_fp8_cache_argument_errors(lib):
     assert _call(lib, p) != binding.DA_ERR_UNSUPPORTED
 
 
+def test_test_hook_flag_is_accepted(lib):
+    p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 0, 0, 0, 64, False)
+    p.flags = binding.DA_FLAG_TEST_WITHHOLD_COPY | binding.DA_FLAG_TWO_PASS
+    assert _call(lib, p) != -2                    # not an unknown flag
+
+
 def test_paging_errors(lib):
     p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 24, 4, 10, 64, False)
     assert _call(lib, p, bt=16) == -4           # page size not a multiple of 16

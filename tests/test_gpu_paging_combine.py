@@ -284,3 +284,33 @@ def test_wide_and_fp8_calls_replay_inside_a_cuda_graph(binding, kind):
     ref_o, ref_l = oracle.decode_attention_inputs(inp)
     assert_out_close(bf16_tensor_to_f64(out), ref_o)
     assert_lse_close(lse.cpu().numpy(), ref_l)
+
+
+
+def test_withheld_copy_times_out_and_context_stays_usable(binding):
+    """Failure detection without a GPU fault: the test flag makes block
+    (0, 0, 0) of the split launch withhold its first pipeline stage, so that
+    block's bounded wait runs out (~2 s) and the call reports
+    DA_STATUS_TIMEOUT; the next call on the same context is exact."""
+    import time
+    shp = W.small_shape("withhold", batch=2, num_q_heads=8, num_kv_heads=2, lo=500, hi=900,
+                        seed=70)
+    inp = W.make_host_inputs(shp)
+    q, k, v, bt, lens = to_device(inp)
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, two_pass=True)
+    p.flags |= binding.DA_FLAG_TEST_WITHHOLD_COPY
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len, num_splits=2,
+                        status=status, params=p)
+    torch.cuda.synchronize()
+    assert int(status.item()) & binding.DA_STATUS_TIMEOUT
+    assert time.time() - t0 < 60
+    status.zero_()
+    out, lse = binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len,
+                                   num_splits=2, status=status, two_pass=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle.decode_attention_inputs(inp)
+    assert_out_close(bf16_tensor_to_f64(out), ref_o)
+    assert_lse_close(lse.cpu().numpy(), ref_l)
