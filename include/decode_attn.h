@@ -47,7 +47,7 @@
  * (quantisation with explicit scaling factors rather than a plain cast:
  * "Capstone FlashAttention", §2.2 FP8 with scaling; the CUTLASS split-KV post,
  * §5.8).  q, out and lse keep their types.  Strides are then in bytes and must
- * be multiples of 16; at most 16 rows per kv head ((Hq/Hkv)*q_len).
+ * be multiples of 16.
  *
  * Ownership and errors.  The caller owns every buffer (device memory unless
  * stated otherwise), including the workspace.  The library allocates nothing
@@ -91,8 +91,8 @@ extern "C" {
 #define DA_ERR_NO_DEVICE -9        /* no usable sm_103 device is current */
 #define DA_ERR_SPLITS -10          /* num_splits out of range */
 #define DA_ERR_STATIC_WORKSPACE_LIMIT -11 /* partials exceed the static workspace */
-#define DA_ERR_UNSUPPORTED -12     /* a flag combination this library does not run:
-                                      FP8 caches with more than 16 rows per kv head */
+#define DA_ERR_UNSUPPORTED -12     /* a flag combination this library does not run
+                                      (reserved: no combination returns it at present) */
 
 /* size of the device array behind decode_attn_static_workspace() */
 #define DECODE_ATTN_STATIC_WORKSPACE_BYTES (16u << 20)

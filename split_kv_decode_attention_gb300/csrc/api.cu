@@ -95,7 +95,6 @@ int check_shape(const decode_attn_params* p) {
   if (p->head_dim != DECODE_ATTN_HEAD_DIM) return DA_ERR_HEAD_DIM;
   if (static_cast<int64_t>(p->num_q_heads / p->num_kv_heads) * p->q_len > DECODE_ATTN_MAX_ROWS)
     return DA_ERR_ROWS;
-  if (kv_fp8(p) && rows_of(p) > dattn::kMaxNarrowRows) return DA_ERR_UNSUPPORTED;
   return DA_OK;
 }
 
@@ -484,7 +483,7 @@ const char* decode_attn_status_string(int code) {
     case DA_ERR_NO_DEVICE: return "no usable sm_100-class device is current";
     case DA_ERR_SPLITS: return "num_splits / chunk_len out of range";
     case DA_ERR_UNSUPPORTED:
-      return "FP8 caches run with at most 16 rows per kv head ((Hq/Hkv) * q_len)";
+      return "a flag combination this library does not run";
     case DA_ERR_STATIC_WORKSPACE_LIMIT:
       return "the call's partials exceed the 16 MiB static workspace (use fewer splits or decode_attn with a workspace)";
     default: return "unknown status code";

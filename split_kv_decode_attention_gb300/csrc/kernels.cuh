@@ -34,7 +34,7 @@ struct SplitArgs {
   int causal;
   float scale_log2;                    // softmax scale * log2(e)
   int persistent;                      // wide kernel: CTAs walk an item list (set by its launcher)
-  int kv_fp8;                          // caches hold FP8 E4M3 (narrow kernel only)
+  int kv_fp8;                          // caches hold FP8 E4M3
   float v_scale;                       // FP8: values = v_scale * V (k_scale is in scale_log2)
   int test_withhold;                   // DA_FLAG_TEST_WITHHOLD_COPY (narrow kernel, two-pass)
 };

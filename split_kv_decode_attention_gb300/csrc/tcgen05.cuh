@@ -24,12 +24,14 @@ __device__ __forceinline__ uint64_t umma_smem_desc(uint32_t smem_byte_addr, uint
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
-// a_mn / b_mn select an MN-major (instead of K-major) operand.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+// Instruction descriptor of tcgen05.mma kind::f16 with bf16 (or, with f16 =
+// true, f16) A/B and fp32 D.  a_mn / b_mn select an MN-major (instead of
+// K-major) operand.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn, bool b_mn,
+                                                       bool f16 = false) {
   return (1u << 4)                                   // D format: f32
-         | (1u << 7)                                 // A format: bf16
-         | (1u << 10)                                // B format: bf16
+         | (f16 ? 0u : (1u << 7))                    // A format: bf16 (1) or f16 (0)
+         | (f16 ? 0u : (1u << 10))                   // B format: bf16 (1) or f16 (0)
          | (a_mn ? (1u << 15) : 0u)                  // A major
          | (b_mn ? (1u << 16) : 0u)                  // B major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8

@@ -53,43 +53,73 @@ constexpr int kWTiles = kWTok / kTileTokens; // 16-token page tiles per stage
 #ifndef DATTN_WIDE_STAGES
 #define DATTN_WIDE_STAGES 5
 #endif
-constexpr int kWStages = DATTN_WIDE_STAGES;  // K/V stages in flight
 #ifndef DATTN_WIDE_PRODUCERS
 #define DATTN_WIDE_PRODUCERS 5
 #endif
-// TMA copies issued by one warp are serialised (~130 cycles per box), so
-// several producer warps share each stage's boxes.
-constexpr int kWProducers = DATTN_WIDE_PRODUCERS;
-constexpr int kWProducerWarp = 8;            // warps 0-7 softmax (2 groups), then TMA, then MMA
-constexpr int kWMmaWarp = kWProducerWarp + kWProducers;
-constexpr int kWThreads = 32 * (kWMmaWarp + 1);
-constexpr int kWBoxes = 4 * kWTiles;         // per stage: tiles x {K, V} x 2 d-halves, 2 KB each
-constexpr int kWBoxesPerWarp = (kWBoxes + kWProducers - 1) / kWProducers;
-static_assert(kWProducers >= 1 && kWBoxesPerWarp <= 32, "boxes per producer warp");
+#ifndef DATTN_WIDE_F8_STAGES
+#define DATTN_WIDE_F8_STAGES 4
+#endif
+#ifndef DATTN_WIDE_F8_PRODUCERS
+#define DATTN_WIDE_F8_PRODUCERS 2
+#endif
+#ifndef DATTN_WIDE_F8_CONVERTERS
+#define DATTN_WIDE_F8_CONVERTERS 5
+#endif
+#ifndef DATTN_WIDE_F8_OPS
+#define DATTN_WIDE_F8_OPS 3
+#endif
 constexpr int kWSoftmaxThreads = 256;
-constexpr int kWHalf = kWTok * 128;          // [64 tokens][64 d] bf16 = 8 KB
-constexpr int kWStageBytes = 4 * kWHalf;     // K halves, then V halves
+constexpr int kWHalf = kWTok * 128;          // [64 tokens][64 d] 16-bit = 8 KB
+constexpr int kWStageBytes = 4 * kWHalf;     // operand stage: K halves, then V halves
+constexpr int kWF8Tile = kTileTokens * 128;  // one FP8 tile (K or V): 16 rows of 128 bytes
 // Requests whose schedule tables fit in shared memory (else one item per
 // CTA), and up to which the partial chunks are sorted by length.
 constexpr int kWMaxSchedBatch = 1024;
 constexpr int kWSortBatch = 256;
-// Shared memory: K/V ring, Q staging ([128 rows][16 chunks of 16 B], chunk c
-// of row r at c ^ (r & 15)), the groups' merge statistics (two buffers),
-// schedule tables (clamped lengths, prefix of full chunks, partial order,
-// totals), barriers.
-constexpr int kWOffStage = 0;
-constexpr int kWOffQ = kWOffStage + kWStages * kWStageBytes;
-constexpr int kWOffStat = kWOffQ + kWRows * 256;
 constexpr int kWStatFloats = 4 * kWRows + 2;       // m, l per group and row; ok per group
 constexpr int kWStatBytes = 2560;
-constexpr int kWOffSched = kWOffStat + 2 * kWStatBytes;
 constexpr int kWSchedInts = 4 * kWMaxSchedBatch + 4;
-constexpr int kWOffBar = kWOffSched + ((kWSchedInts * 4 + 15) & ~15);
-// full[], empty[], then s_full, s_free, p_full, pv_done per group, q_full, q_empty, item_go
-constexpr int kWNumBars = 2 * kWStages + 8 + 3;
-constexpr int kWSmemBytes = 1024 + kWOffBar + kWNumBars * 8 + 16;
 static_assert(kWStatFloats * 4 <= kWStatBytes, "statistics buffer");
-static_assert(kWSmemBytes <= 227 * 1024, "shared memory");
+
+// Warp roles and shared-memory layout of the two variants.
+//   bf16 caches: warps 0-7 softmax, 8..12 TMA producers, 13 MMA; the TMA ring
+//     holds the MMA operands directly (5 stages of 32 KB).
+//   FP8 caches: warps 0-7 softmax, 8..9 TMA producers, 10..14 converters,
+//     15 MMA; the TMA ring holds FP8 stages (4 x 16 KB: 8 boxes of 2 KB per 64
+//     keys), the converters widen each to an f16 operand stage in a 3-slot
+//     ring (the B operands of kind::f16 must be 16-bit).
+// Shared memory: TMA ring, operand ring (FP8 only), Q staging ([128 rows][16
+// chunks of 16 B], chunk c of row r at c ^ (r & 15)), the groups' merge
+// statistics (two buffers), schedule tables, barriers.
+// TMA copies issued by one warp are serialised (~130 cycles per box), so
+// several producer warps share each stage's boxes.
+template <bool F8>
+struct WCfg {
+  static constexpr int kProducers = F8 ? DATTN_WIDE_F8_PRODUCERS : DATTN_WIDE_PRODUCERS;
+  static constexpr int kConverters = F8 ? DATTN_WIDE_F8_CONVERTERS : 0;
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kConverterWarp = kProducerWarp + kProducers;
+  static constexpr int kMmaWarp = kConverterWarp + kConverters;
+  static constexpr int kThreads = 32 * (kMmaWarp + 1);
+  static constexpr int kStages = F8 ? DATTN_WIDE_F8_STAGES : DATTN_WIDE_STAGES;  // TMA ring
+  static constexpr int kLoadBytes = F8 ? 2 * kWTiles * kWF8Tile : kWStageBytes;
+  static constexpr int kBoxes = F8 ? 2 * kWTiles : 4 * kWTiles;  // 2 KB boxes per stage
+  static constexpr int kBoxesPerWarp = (kBoxes + kProducers - 1) / kProducers;
+  static constexpr int kOpStages = F8 ? DATTN_WIDE_F8_OPS : kStages;  // stages the MMA reads
+  static constexpr int kOffLoad = 0;
+  static constexpr int kOffOp = F8 ? kOffLoad + kStages * kLoadBytes : kOffLoad;
+  static constexpr int kOffQ = F8 ? kOffOp + kOpStages * kWStageBytes : kOffLoad + kStages * kLoadBytes;
+  static constexpr int kOffStat = kOffQ + kWRows * 256;
+  static constexpr int kOffSched = kOffStat + 2 * kWStatBytes;
+  static constexpr int kOffBar = kOffSched + ((kWSchedInts * 4 + 15) & ~15);
+  // full[], empty[] of the TMA ring, conv_full[], conv_empty[] of the operand
+  // ring (FP8), then s_full, s_free, p_full, pv_done per group, q_full,
+  // q_empty, item_go
+  static constexpr int kNumBars = 2 * kStages + (F8 ? 2 * kOpStages : 0) + 8 + 3;
+  static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
+  static_assert(kProducers >= 1 && kBoxesPerWarp <= 32, "boxes per producer warp");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
 // Tensor memory (512 columns x 128 lanes, lane = query row): fp32 scores
 // S[g] at 64 g, fp32 outputs O[g] at 128 + 128 g, bf16 probabilities P[g]
 // (64 keys packed in 32 columns) at 384 + 32 g, and the bf16 query rows Q
@@ -186,9 +216,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // P.V accumulates into O[g]; the two groups alternate, so one group's softmax
 // overlaps the other's, and their (m, l, O) merge exactly at the end.  Phases
 // of the ring and of each group's barriers run on across items.
-__global__ void __launch_bounds__(kWThreads, 1)
+template <bool F8>
+__global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     wide_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                 const SplitArgs a) {
+  using C = WCfg<F8>;
   constexpr uint32_t kFull = 0xffffffffu;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -219,18 +251,20 @@ __global__ void __launch_bounds__(kWThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWOffBar);
-  uint64_t* full_bar = bars;                   // [kWStages] TMA bytes landed
-  uint64_t* empty_bar = bars + kWStages;       // [kWStages] stage consumed by the MMAs
-  uint64_t* s_full = bars + 2 * kWStages;      // [2] scores in TMEM buffer
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full_bar = bars;                   // [kStages] TMA bytes landed
+  uint64_t* empty_bar = bars + C::kStages;     // [kStages] TMA slot free again
+  uint64_t* conv_full = empty_bar + C::kStages;                     // FP8: operand stage widened
+  uint64_t* conv_empty = conv_full + (F8 ? C::kOpStages : 0);       // FP8: operand stage consumed
+  uint64_t* s_full = conv_empty + (F8 ? C::kOpStages : 0);          // [2] scores in TMEM buffer
   uint64_t* s_free = s_full + 2;               // [2] score buffer read by softmax
   uint64_t* p_full = s_free + 2;               // [2] P buffer (and O rescale) ready for PV
   uint64_t* pv_done = p_full + 2;              // [2] PV of that P buffer finished
   uint64_t* q_full = pv_done + 2;              // Q rows of the next item staged
   uint64_t* q_empty = q_full + 1;              // staging copied into TMEM
   uint64_t* item_go = q_empty + 1;             // Q in TMEM, previous outputs read (items with keys)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kWNumBars);
-  int* sched = reinterpret_cast<int*>(smem + kWOffSched);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  int* sched = reinterpret_cast<int*>(smem + C::kOffSched);
   int* s_len = sched + kWSchLen;
   int* s_fpre = sched + kWSchFpre;
   int* s_pord = sched + kWSchPord;
@@ -238,9 +272,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
   int* s_rem = sched + kWSchRem;
 
   if (tid == 0) {
-    for (int s = 0; s < kWStages; ++s) {
-      mbar_init(&full_bar[s], kWProducers);
-      mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], C::kProducers);
+      mbar_init(&empty_bar[s], F8 ? C::kConverters : 1);
+    }
+    if (F8) {
+      for (int o = 0; o < C::kOpStages; ++o) {
+        mbar_init(&conv_full[o], C::kConverters);
+        mbar_init(&conv_empty[o], 1);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -248,13 +288,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(q_full, 32 * kWProducers);
+    mbar_init(q_full, 32 * C::kProducers);
     mbar_init(q_empty, 4);
     mbar_init(item_go, 8);
     fence_mbar_init();
     s_tot[2] = L0;
   }
-  if (warp == kWMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(tmem_slot, kWTmemCols);
     tmem_relinquish();
   }
@@ -263,7 +303,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   // per request (scanned by warp 0), partial chunks ordered longest first
   const int chunk = a.chunk_len;
   if (persistent) {
-    for (int b = tid; b < a.batch; b += kWThreads) {
+    for (int b = tid; b < a.batch; b += C::kThreads) {
       int L = b == tid ? L_first : a.seq_lens[b];
       uint32_t bad = 0;
       if (L < 0 || L > a.max_seq_len) {
@@ -317,7 +357,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (a.batch <= kWSortBatch) {
       // rank of each partial chunk among all partial chunks: longer first,
       // ties by request index
-      for (int b = tid; b < a.batch; b += kWThreads) {
+      for (int b = tid; b < a.batch; b += C::kThreads) {
         const int rem = s_rem[b];
         if (rem == chunk) continue;
         int rank = 0;
@@ -336,14 +376,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const uint32_t smem_base = smem_addr(smem);
 
   // ============================================================ TMA producer
-  if (warp >= kWProducerWarp && warp < kWMmaWarp) {
-    const int pw_idx = warp - kWProducerWarp;
+  if (warp >= C::kProducerWarp && warp < C::kConverterWarp) {
+    const int pw_idx = warp - C::kProducerWarp;
     if (lane == 0 && pw_idx == 0 && a.max_seq_len > 0) {
       prefetch_tensor_map(&k_map);
       prefetch_tensor_map(&v_map);
     }
     const uint64_t policy = l2_evict_first_policy();
-    const uint32_t q_stage = smem_base + kWOffQ;
+    const uint32_t q_stage = smem_base + C::kOffQ;
     int gs = 0;  // stages issued so far (all items)
     bool ok = true;
     Item it;
@@ -357,7 +397,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           break;
         }
       }
-      for (int r = pw_idx * 32 + lane; r < a.rows; r += 32 * kWProducers) {
+      for (int r = pw_idx * 32 + lane; r < a.rows; r += 32 * C::kProducers) {
         const int t = r / a.group;
         const uint16_t* qrow = a.q + static_cast<int64_t>(it.b) * a.q_sb +
                                static_cast<int64_t>(t) * a.q_st +
@@ -374,8 +414,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       PageWindow pw{bt_row, it.t_begin, it.n_tiles, a.page_size, a.num_pages, lane, a.status, 0, 0, 0};
       if (a.paged) pw.init();
       for (int i = 0; i < it.n_iters; ++i, ++gs) {
-        const int s = gs % kWStages;
-        const int use = gs / kWStages;
+        const int s = gs % C::kStages;
+        const int use = gs / C::kStages;
         int good = 1;
         if (lane == 0 && use > 0) good = mbar_wait_spin(&empty_bar[s], (use - 1) & 1) ? 1 : 0;
         good = __shfl_sync(kFull, good, 0);
@@ -384,29 +424,33 @@ __global__ void __launch_bounds__(kWThreads, 1)
           break;
         }
         const int tiles_here = min(kWTiles, it.n_tiles - i * kWTiles);
-        // this lane's box: bx = lane * kWProducers + pw_idx (tile bx / 4; K or
-        // V and the d-half from bx % 4); page id of its tile picked in registers
-        const int bx = lane * kWProducers + pw_idx;
+        // this lane's box: bx = lane * kProducers + pw_idx -- bf16: tile bx / 4,
+        // K or V and the d-half from bx % 4; FP8: tile bx / 2, K or V from
+        // bx % 2 (one box holds all 128 d); page id of its tile picked in registers
+        constexpr int kPerTile = F8 ? 2 : 4;
+        const int bx = lane * C::kProducers + pw_idx;
         int my_pg = 0;
 #pragma unroll
         for (int ti = 0; ti < kWTiles; ++ti) {
           const int pg = a.paged ? pw.get(i * kWTiles + ti) : 0;
-          if ((bx >> 2) == ti) my_pg = pg;
+          if (bx / kPerTile == ti) my_pg = pg;
         }
         // boxes of this warp that hold data (tiles past the chunk end are skipped)
         int mine = 0;
-        for (int c = pw_idx; c < tiles_here * 4; c += kWProducers) ++mine;
+        for (int c = pw_idx; c < tiles_here * kPerTile; c += C::kProducers) ++mine;
         if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(mine * 2048));
         __syncwarp();
-        if (lane < kWBoxesPerWarp && bx < tiles_here * 4) {
-          const int ti = bx >> 2;
+        if (lane < C::kBoxesPerWarp && bx < tiles_here * kPerTile) {
+          const int ti = bx / kPerTile;
           const int tok = it.t_begin + (i * kWTiles + ti) * kTileTokens;
           const int grp = a.paged ? my_pg : it.b;
           const int tin = a.paged ? tok % a.page_size : tok;
-          const int half = bx & 1;
-          const bool is_v = (bx & 2) != 0;
-          uint8_t* dst = smem + kWOffStage + s * kWStageBytes + (is_v ? 2 * kWHalf : 0) +
-                         half * kWHalf + ti * 2048;
+          const int half = F8 ? 0 : (bx & 1);
+          const bool is_v = F8 ? (bx & 1) != 0 : (bx & 2) != 0;
+          uint8_t* dst = F8 ? smem + C::kOffLoad + s * C::kLoadBytes +
+                                  (is_v ? kWTiles * kWF8Tile : 0) + ti * kWF8Tile
+                            : smem + C::kOffLoad + s * C::kLoadBytes + (is_v ? 2 * kWHalf : 0) +
+                                  half * kWHalf + ti * 2048;
           tma_load_4d(dst, is_v ? &v_map : &k_map, &full_bar[s], half * 64, it.kvh, tin, grp,
                       policy);
         }
@@ -416,43 +460,112 @@ __global__ void __launch_bounds__(kWThreads, 1)
     cp_async_wait_all();
     if (lane == 0) {
       if (!ok && a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
-      for (int g = max(0, gs - kWStages); g < gs; ++g)
-        mbar_wait(&full_bar[g % kWStages], (g / kWStages) & 1);
+      for (int g = max(0, gs - C::kStages); g < gs; ++g)
+        mbar_wait(&full_bar[g % C::kStages], (g / C::kStages) & 1);
     }
+    return;
+  }
+
+  // ======================================================= FP8 converters
+  // Widen each landed FP8 stage to an f16 operand stage ([2 d-halves][64
+  // tokens][64 d], 128-byte swizzle): 16-byte chunk c of FP8 row t (d = 16c ..
+  // 16c+15) becomes 8-d chunks 2c and 2c+1 of d-half c / 4.  Each 8-lane
+  // phase takes one chunk index of 8 consecutive rows, so loads (slot c ^ j)
+  // and stores ((2c & 7) ^ j, and ^ 1) hit 8 distinct bank groups.
+  if (F8 && warp >= C::kConverterWarp && warp < C::kMmaWarp) {
+    const int ct = tid - 32 * C::kConverterWarp;
+    int gs = 0;
+    bool ok = true;
+    Item it;
+    for (int k = 0; ok && schedule_item(sched, a, k, &it); ++k) {
+      for (int i = 0; i < it.n_iters; ++i, ++gs) {
+        const int s = gs % C::kStages;
+        const int o = gs % C::kOpStages;
+        ok = __all_sync(kFull, mbar_wait(&full_bar[s], (gs / C::kStages) & 1)) != 0;
+        if (ok && gs >= C::kOpStages)
+          ok = __all_sync(kFull, mbar_wait(&conv_empty[o], ((gs / C::kOpStages) - 1) & 1)) != 0;
+        if (!ok) break;
+        const uint8_t* src = smem + C::kOffLoad + s * C::kLoadBytes;
+        uint8_t* dst = smem + C::kOffOp + o * kWStageBytes;
+        // item idx: (K or V, tile, 8-row block, chunk c, row j); four loads in
+        // flight before the conversions
+        constexpr int kItems = 2 * kWTiles * 128;
+        constexpr int kCT = 32 * C::kConverters;
+#pragma unroll
+        for (int k0 = 0; k0 < (kItems + kCT - 1) / kCT; k0 += 4) {
+          uint4 raw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int idx = ct + (k0 + u) * kCT;
+            if (idx < kItems) {
+              const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
+              const int ti = (idx >> 7) & (kWTiles - 1), kv = idx >> 9;
+              raw[u] = *reinterpret_cast<const uint4*>(src + kv * kWTiles * kWF8Tile + ti * kWF8Tile +
+                                                       tin * 128 + ((c ^ j) << 4));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int idx = ct + (k0 + u) * kCT;
+            if (idx < kItems) {
+              const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
+              const int ti = (idx >> 7) & (kWTiles - 1), kv = idx >> 9;
+              uint8_t* row =
+                  dst + kv * 2 * kWHalf + (c >> 2) * kWHalf + (ti * kTileTokens + tin) * 128;
+              const int c0 = (2 * c) & 7;
+              *reinterpret_cast<uint4*>(row + ((c0 ^ j) << 4)) =
+                  make_uint4(e4m3x2_to_f16x2(raw[u].x), e4m3x2_to_f16x2(raw[u].x >> 16),
+                             e4m3x2_to_f16x2(raw[u].y), e4m3x2_to_f16x2(raw[u].y >> 16));
+              *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ j) << 4)) =
+                  make_uint4(e4m3x2_to_f16x2(raw[u].z), e4m3x2_to_f16x2(raw[u].z >> 16),
+                             e4m3x2_to_f16x2(raw[u].w), e4m3x2_to_f16x2(raw[u].w >> 16));
+            }
+          }
+        }
+        fence_proxy_async_smem();  // the tensor core reads the widened stage
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&conv_full[o]);
+          mbar_arrive(&empty_bar[s]);
+        }
+      }
+    }
+    if (!ok && lane == 0 && a.status != nullptr)
+      atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
     return;
   }
 
   // ============================================================= MMA issuer
   // The whole warp runs this loop (all its values warp-uniform) and one
   // elected lane issues each MMA and commit.
-  if (warp == kWMmaWarp) {
-    constexpr uint32_t kIdescQK = umma_idesc_bf16(kWRows, kWTok, false, false);
-    constexpr uint32_t kIdescPV = umma_idesc_bf16(kWRows, kHeadDim, false, true);
+  if (warp == C::kMmaWarp) {
+    constexpr uint32_t kIdescQK = umma_idesc_bf16(kWRows, kWTok, false, false, F8);
+    constexpr uint32_t kIdescPV = umma_idesc_bf16(kWRows, kHeadDim, false, true, F8);
     // B-operand descriptors of stage 0: other stages and K-steps differ only
     // in the start-address field (16-byte units, no carry below 256 KB), so
     // each MMA adds a constant to one of these. A (Q, P) is read from TMEM.
-    const uint64_t k_desc0 = umma_smem_desc(smem_base + kWOffStage, 16, 1024);
+    const uint64_t k_desc0 = umma_smem_desc(smem_base + C::kOffOp, 16, 1024);
     // B = V [64 keys][2 x 64 d], MN-major: d-halves 8 KB apart (LBO), 8-key
     // groups 1 KB apart (SBO), 16 keys = 2 KB per K-step
-    const uint64_t v_desc0 = umma_smem_desc(smem_base + kWOffStage + 2 * kWHalf, kWHalf, 1024);
+    const uint64_t v_desc0 = umma_smem_desc(smem_base + C::kOffOp + 2 * kWHalf, kWHalf, 1024);
     // O += P_jj . V_jj (ring stage gsj), then release the stage and the P buffer
     auto issue_pv = [&](int jj, int gsj) {
       tc_fence_after_sync();
       const uint32_t pa = tmem + kWColP + (jj & 1) * (kWTok / 2);
-      const uint64_t vd = v_desc0 + static_cast<uint64_t>((gsj % kWStages) * (kWStageBytes >> 4));
+      const uint64_t vd = v_desc0 + static_cast<uint64_t>((gsj % C::kOpStages) * (kWStageBytes >> 4));
       const uint32_t d = tmem + kWColO + (jj & 1) * kHeadDim;
 #pragma unroll
       for (int kk = 0; kk < kWTok / 16; ++kk)  // 16 keys = 8 P columns per K-step
         umma_bf16_ts_warp(d, pa + kk * 8, vd + kk * (2048 >> 4), kIdescPV,
                           (jj > 1 || kk > 0) ? 1u : 0u);
       umma_commit_warp(&pv_done[jj & 1]);
-      umma_commit_warp(&empty_bar[gsj % kWStages]);
+      umma_commit_warp(F8 ? &conv_empty[gsj % C::kOpStages] : &empty_bar[gsj % C::kStages]);
     };
     // S_j = Q . K_j^T: 16 d per K-step (8 Q columns; K: d-half kk / 4, 32
     // bytes into its 128-byte swizzled rows)
     auto issue_qk = [&](int j, int gsj) {
       tc_fence_after_sync();
-      const uint64_t kd = k_desc0 + static_cast<uint64_t>((gsj % kWStages) * (kWStageBytes >> 4));
+      const uint64_t kd = k_desc0 + static_cast<uint64_t>((gsj % C::kOpStages) * (kWStageBytes >> 4));
       const uint32_t d = tmem + (j & 1) * kWTok;
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
@@ -484,7 +597,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
           const int j = next_qk;
           const int gsj = gs + j;
           const int u = ((j & 1) ? u1 : u0) + (j >> 1);  // the group's use of its buffers
-          const bool landed = mbar_test(&full_bar[gsj % kWStages], (gsj / kWStages) & 1);
+          const bool landed = F8 ? mbar_test(&conv_full[gsj % C::kOpStages], (gsj / C::kOpStages) & 1)
+                                 : mbar_test(&full_bar[gsj % C::kStages], (gsj / C::kStages) & 1);
           const bool s_ready = u == 0 || mbar_test(&s_free[j & 1], (u - 1) & 1);
           if (__any_sync(kFull, landed) && __any_sync(kFull, s_ready)) {
             issue_qk(j, gsj);
@@ -531,7 +645,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   const int r = tid & 127;         // query row = TMEM lane
   const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const uint32_t o_col = kWColO + grp * kHeadDim;
-  const uint8_t* q_stage = smem + kWOffQ + r * 256;
+  const uint8_t* q_stage = smem + C::kOffQ + r * 256;
   int gs = 0;      // ring stages of all previous items
   int u_base = 0;  // this group's tiles in all previous items
   bool ok = true;
@@ -558,10 +672,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const uint4 v = r < a.rows
                                 ? *reinterpret_cast<const uint4*>(q_stage + ((ch ^ (r & 15)) << 4))
                                 : make_uint4(0, 0, 0, 0);
-            w[4 * c] = v.x;
-            w[4 * c + 1] = v.y;
-            w[4 * c + 2] = v.z;
-            w[4 * c + 3] = v.w;
+            // FP8 caches: the products run in f16, so Q is widened too
+            w[4 * c] = F8 ? bf16x2_to_f16x2(v.x) : v.x;
+            w[4 * c + 1] = F8 ? bf16x2_to_f16x2(v.y) : v.y;
+            w[4 * c + 2] = F8 ? bf16x2_to_f16x2(v.z) : v.z;
+            w[4 * c + 3] = F8 ? bf16x2_to_f16x2(v.w) : v.w;
           }
           tmem_st16(lane_base + kWColQ + qc * 16, w);
         }
@@ -632,7 +747,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         const float p0 = ex2(x[i] - mref);
         const float p1 = ex2(x[i + 1] - mref);
         psum += p0 + p1;
-        pk[i / 2] = pack_bf16x2(p0, p1);
+        pk[i / 2] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
       }
       l = l * alpha + psum;
 
@@ -667,7 +782,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       // NaN), so zero them before the MMA reads the stage
       const int n_valid = min(kWTok, t_end - tok0);
       if (n_valid < kWTok) {
-        uint8_t* vst = smem + kWOffStage + ((gs + j) % kWStages) * kWStageBytes + 2 * kWHalf;
+        uint8_t* vst = smem + C::kOffOp + ((gs + j) % C::kOpStages) * kWStageBytes + 2 * kWHalf;
         for (int idx = r; idx < (kWTok - n_valid) * 16; idx += 128) {
           const int row = n_valid + (idx >> 4);
           const int c = idx & 15;  // 8 chunks per half, 2 halves
@@ -691,7 +806,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // ---- merge the two groups (same recurrence as the combine) and write
     // O / l (final bf16 row or fp32 partial) and the LSE; group g writes the
     // d-columns [64 g, 64 g + 64) of every row
-    float* stat = reinterpret_cast<float*>(smem + kWOffStat + (k & 1) * kWStatBytes);
+    float* stat = reinterpret_cast<float*>(smem + C::kOffStat + (k & 1) * kWStatBytes);
     tc_fence_before_sync();
     named_barrier_sync(4, kWSoftmaxThreads);  // both groups' last P.V are done
     stat[grp * 256 + r] = m_used;
@@ -707,7 +822,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const float f0 = l0 > 0.f ? ex2(m0 - Mu) : 0.f;
     const float f1 = l1 > 0.f ? ex2(m1 - Mu) : 0.f;
     const float Lt = l0 * f0 + l1 * f1;
-    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    const float inv = (Lt > 0.f ? 1.f / Lt : 0.f) * (F8 ? a.v_scale : 1.f);
     const bool have0 = ok && n_iters > 0;  // O[0] / O[1] were written
     const bool have1 = ok && n_iters > 1;
     const bool direct = it.nsplit == 1;
@@ -765,32 +880,33 @@ __global__ void __launch_bounds__(kWThreads, 1)
 }
 
 std::mutex g_wide_mu;
-bool g_wide_attr[64];
+bool g_wide_attr[2][64];
 int g_wide_sms[64];
 
+template <bool F8>
 cudaError_t ensure_wide_attrs(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_wide_mu);
-  if (!g_wide_attr[dev]) {
-    e = cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmemBytes);
+  if (!g_wide_attr[F8][dev]) {
+    e = cudaFuncSetAttribute(wide_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             WCfg<F8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&g_wide_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    g_wide_attr[dev] = true;
+    g_wide_attr[F8][dev] = true;
   }
   if (sms != nullptr) *sms = g_wide_sms[dev];
   return cudaSuccess;
 }
 
-}  // namespace
-
-cudaError_t launch_wide(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
-                        cudaStream_t stream) {
+template <bool F8>
+cudaError_t launch_wide_t(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
+                          cudaStream_t stream) {
   int sms = 0;
-  cudaError_t e = ensure_wide_attrs(&sms);
+  cudaError_t e = ensure_wide_attrs<F8>(&sms);
   if (e != cudaSuccess) return e;
   SplitArgs pa = a;
   pa.persistent = a.batch <= kWMaxSchedBatch ? 1 : 0;
@@ -799,22 +915,30 @@ cudaError_t launch_wide(const CUtensorMap& k_map, const CUtensorMap& v_map, cons
   const int64_t items = static_cast<int64_t>(a.num_splits) * a.num_kv_heads * a.batch;
   cfg.gridDim = pa.persistent ? dim3(static_cast<unsigned>(std::min<int64_t>(sms, items)))
                               : dim3(a.num_splits, a.num_kv_heads, a.batch);
-  cfg.blockDim = dim3(kWThreads);
-  cfg.dynamicSmemBytes = kWSmemBytes;
+  cfg.blockDim = dim3(WCfg<F8>::kThreads);
+  cfg.dynamicSmemBytes = WCfg<F8>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, wide_kernel, k_map, v_map, pa);
+  return cudaLaunchKernelEx(&cfg, wide_kernel<F8>, k_map, v_map, pa);
+}
+
+}  // namespace
+
+cudaError_t launch_wide(const CUtensorMap& k_map, const CUtensorMap& v_map, const SplitArgs& a,
+                        cudaStream_t stream) {
+  return a.kv_fp8 ? launch_wide_t<true>(k_map, v_map, a, stream)
+                  : launch_wide_t<false>(k_map, v_map, a, stream);
 }
 
 int wide_ctas_per_sm() {
-  if (ensure_wide_attrs(nullptr) != cudaSuccess) return 1;
+  if (ensure_wide_attrs<false>(nullptr) != cudaSuccess) return 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wide_kernel, kWThreads, kWSmemBytes) !=
-          cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wide_kernel<false>, WCfg<false>::kThreads,
+                                                    WCfg<false>::kSmemBytes) != cudaSuccess ||
       n < 1)
     return 1;
   return n;

@@ -129,7 +129,7 @@ WIDE_WORKLOADS = {
 }
 WORKLOADS.update(WIDE_WORKLOADS)
 
-# FP8 E4M3 caches: the c2 and c5 recipes with the cache quantised per tensor.
+# FP8 E4M3 caches: the c2, c5 and w64 recipes with the cache quantised per tensor.
 FP8_WORKLOADS = {
     "f2_b1_mha32_L131072_fp8": DecodeShape(
         "f2_b1_mha32_L131072_fp8", batch=1, q_len=1, num_q_heads=32, num_kv_heads=32,
@@ -138,6 +138,10 @@ FP8_WORKLOADS = {
         "f5_b32_q4_causal_h32kv8_L1024-16384_paged_fp8", batch=32, q_len=4,
         num_q_heads=32, num_kv_heads=8, seq_len_lo=1024, seq_len_hi=16384,
         paged=True, causal=True, seed=1009, kv_fp8=True),
+    "fw64_b32_q8_h64kv8_causal_L1024-16384_paged_fp8": DecodeShape(
+        "fw64_b32_q8_h64kv8_causal_L1024-16384_paged_fp8", batch=32, q_len=8,
+        num_q_heads=64, num_kv_heads=8, seq_len_lo=1024, seq_len_hi=16384,
+        paged=True, causal=True, seed=1010, kv_fp8=True),
 }
 WORKLOADS.update(FP8_WORKLOADS)
 

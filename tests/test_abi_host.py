@@ -90,8 +90,8 @@ def test_null_and_alignment_errors(lib):
 
 
 def test_fp8_cache_argument_errors(lib):
-    """FP8 E4M3 caches: byte strides must be multiples of 16, the scales finite,
-    and at most 16 rows per kv head run (the tcgen05 kernel reads bf16 only)."""
+    """FP8 E4M3 caches: byte strides must be multiples of 16 and the scales
+    finite; every row count up to 128 runs (both kernels read FP8)."""
     p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 0, 0, 0, 64, False)
     p.flags = binding.DA_FLAG_KV_FP8_E4M3
     p.kv_stride_token = 2 * 128 + 8               # a multiple of 8 but not of 16 bytes
@@ -102,10 +102,7 @@ def test_fp8_cache_argument_errors(lib):
     assert _call(lib, p) == -2
     p = binding.decode_attn_params_init(1, 4, 64, 8, 128, 0, 0, 0, 64, True)  # 8 x 4 = 32 rows
     p.flags = binding.DA_FLAG_KV_FP8_E4M3
-    assert _call(lib, p) == binding.DA_ERR_UNSUPPORTED
-    assert "16 rows" in binding.decode_attn_status_string(binding.DA_ERR_UNSUPPORTED)
-    p.flags = 0                                   # the same shape with bf16 caches is fine
-    assert _call(lib, p) != binding.DA_ERR_UNSUPPORTED
+    assert _call(lib, p) not in (-2, -5, -6, binding.DA_ERR_UNSUPPORTED)
 
 
 def test_test_hook_flag_is_accepted(lib):

@@ -249,13 +249,13 @@ def test_call_replays_inside_a_cuda_graph(binding):
 
 
 
-@pytest.mark.parametrize("kind", ["wide", "fp8"])
+@pytest.mark.parametrize("kind", ["wide", "fp8", "fp8_wide"])
 def test_wide_and_fp8_calls_replay_inside_a_cuda_graph(binding, kind):
     """The persistent tcgen05 kernel (64 rows per KV head) and the FP8-cache
-    path captured in a CUDA graph and replayed."""
-    if kind == "wide":
+    paths captured in a CUDA graph and replayed."""
+    if kind in ("wide", "fp8_wide"):
         shp = W.small_shape("graph_w", batch=5, q_len=8, num_q_heads=16, num_kv_heads=2,
-                            lo=100, hi=3000, causal=True, seed=49)
+                            lo=100, hi=3000, causal=True, seed=49, kv_fp8=kind == "fp8_wide")
     else:
         shp = W.small_shape("graph_f8", batch=4, q_len=2, num_q_heads=8, num_kv_heads=2,
                             lo=100, hi=3000, causal=True, seed=50, kv_fp8=True)

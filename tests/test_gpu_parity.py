@@ -199,6 +199,10 @@ FP8_CASES = [
     ("f8_gqa16_paged", 16, 1, False, True, 16, 1, 400),
     ("f8_mha_q16_causal", 1, 16, True, True, 16, 16, 300),
     ("f8_gqa4_q2_page32", 4, 2, True, True, 32, 2, 700),
+    # wide query groups with FP8 caches: the tcgen05 kernel widens them to f16
+    ("f8w32_gqa8_q4_causal", 8, 4, True, True, 16, 4, 900),
+    ("f8w64_gqa16_q4_page32", 16, 4, False, True, 32, 4, 600),
+    ("f8w128_gqa16_q8_causal", 16, 8, True, True, 16, 8, 500),
 ]
 
 
