@@ -15,11 +15,11 @@
 // list is rebuilt by every CTA from seq_lens in shared memory; batches too
 // large for those tables fall back to one item per CTA (grid = chunks x kv
 // heads x requests).  Per CTA:
-//   * warps 8..11 stream K/V with TMA through one ring of 64-token stages
+//   * producer warps stream K/V with TMA through one ring of 64-token stages
 //     (four 16-token page tiles, [2 d-halves][64 tokens][64 d], 128-byte
 //     swizzle, mbarrier byte counts) without stopping between items, and
 //     stage each item's query rows in shared memory with cp.async;
-//   * warp 12 issues the MMAs (one elected lane, warp-uniform operands):
+//   * one warp issues the MMAs (one elected lane, warp-uniform operands):
 //     S = Q.K^T (M = 128 rows padded, N = 64 keys, K = 128 d; A = Q from
 //     TMEM, B = K from shared memory) into one of two TMEM score buffers, and
 //     O += P.V (N = 128 d, K = 64 keys; A = P from TMEM, B = V read MN-major
@@ -91,8 +91,9 @@ static_assert(kWStatFloats * 4 <= kWStatBytes, "statistics buffer");
 // Shared memory: TMA ring, operand ring (FP8 only), Q staging ([128 rows][16
 // chunks of 16 B], chunk c of row r at c ^ (r & 15)), the groups' merge
 // statistics (two buffers), schedule tables, barriers.
-// TMA copies issued by one warp are serialised (~130 cycles per box), so
-// several producer warps share each stage's boxes.
+// TMA copies issued by one warp are serialised (~130-240 cycles per box), and
+// the time to issue a stage counts against its ring slot, so all producer
+// warps share each stage's boxes.
 template <bool F8>
 struct WCfg {
   static constexpr int kProducers = F8 ? DATTN_WIDE_F8_PRODUCERS : DATTN_WIDE_PRODUCERS;
@@ -104,7 +105,6 @@ struct WCfg {
   static constexpr int kStages = F8 ? DATTN_WIDE_F8_STAGES : DATTN_WIDE_STAGES;  // TMA ring
   static constexpr int kLoadBytes = F8 ? 2 * kWTiles * kWF8Tile : kWStageBytes;
   static constexpr int kBoxes = F8 ? 2 * kWTiles : 4 * kWTiles;  // 2 KB boxes per stage
-  static constexpr int kBoxesPerWarp = (kBoxes + kProducers - 1) / kProducers;
   static constexpr int kOpStages = F8 ? DATTN_WIDE_F8_OPS : kStages;  // stages the MMA reads
   static constexpr int kOffLoad = 0;
   static constexpr int kOffOp = F8 ? kOffLoad + kStages * kLoadBytes : kOffLoad;
@@ -117,7 +117,7 @@ struct WCfg {
   // q_empty, item_go
   static constexpr int kNumBars = 2 * kStages + (F8 ? 2 * kOpStages : 0) + 8 + 3;
   static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
-  static_assert(kProducers >= 1 && kBoxesPerWarp <= 32, "boxes per producer warp");
+  static_assert(kProducers >= 1 && kBoxes <= 32 * kProducers, "one box per producer lane");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 // Tensor memory (512 columns x 128 lanes, lane = query row): fp32 scores
@@ -384,7 +384,16 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     }
     const uint64_t policy = l2_evict_first_policy();
     const uint32_t q_stage = smem_base + C::kOffQ;
-    int gs = 0;  // stages issued so far (all items)
+    // this lane's box of every stage
+    constexpr int kPerTile = F8 ? 2 : 4;
+    const int bx = lane * C::kProducers + pw_idx;
+    const int ti = bx / kPerTile;
+    const int half = F8 ? 0 : (bx & 1);
+    const bool is_v = F8 ? (bx & 1) != 0 : (bx & 2) != 0;
+    const int box_off = F8 ? C::kOffLoad + (is_v ? kWTiles * kWF8Tile : 0) + ti * kWF8Tile
+                           : C::kOffLoad + (is_v ? 2 * kWHalf : 0) + half * kWHalf + ti * 2048;
+    int gs = 0;       // stages of all previous items
+    int last_g = -1;  // the last stage this warp issued
     bool ok = true;
     Item it;
     for (int k = 0; ok && schedule_item(sched, a, k, &it); ++k) {
@@ -408,14 +417,23 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       }
       cp_async_arrive(q_full);
 
-      // ---- K/V stages of the item
+      // ---- K/V stages of the item: each producer warp issues its share of
+      // every stage's 2 KB boxes (box bx = lane * kProducers + pw_idx) -- bf16:
+      // tile bx / 4, K or V and the d-half from bx % 4; FP8: tile bx / 2, K or
+      // V from bx % 2 (one box holds all 128 d). Each lane loads the page id
+      // of its next box a stage ahead and checks it when it is used.
       const int32_t* bt_row =
           a.paged ? a.block_table + static_cast<int64_t>(it.b) * a.bt_stride : nullptr;
-      PageWindow pw{bt_row, it.t_begin, it.n_tiles, a.page_size, a.num_pages, lane, a.status, 0, 0, 0};
-      if (a.paged) pw.init();
-      for (int i = 0; i < it.n_iters; ++i, ++gs) {
-        const int s = gs % C::kStages;
-        const int use = gs / C::kStages;
+      auto page_of = [&](int i) -> int {  // raw block-table entry of this lane's tile in stage i
+        const int tile = i * kWTiles + ti;
+        if (bt_row == nullptr || bx >= C::kBoxes || i >= it.n_iters || tile >= it.n_tiles) return 0;
+        return __ldg(bt_row + (it.t_begin + tile * kTileTokens) / a.page_size);
+      };
+      int pg_next = page_of(0);
+      for (int i = 0; i < it.n_iters; ++i) {
+        const int g = gs + i;
+        const int s = g % C::kStages;
+        const int use = g / C::kStages;
         int good = 1;
         if (lane == 0 && use > 0) good = mbar_wait_spin(&empty_bar[s], (use - 1) & 1) ? 1 : 0;
         good = __shfl_sync(kFull, good, 0);
@@ -423,44 +441,36 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
           ok = false;
           break;
         }
-        const int tiles_here = min(kWTiles, it.n_tiles - i * kWTiles);
-        // this lane's box: bx = lane * kProducers + pw_idx -- bf16: tile bx / 4,
-        // K or V and the d-half from bx % 4; FP8: tile bx / 2, K or V from
-        // bx % 2 (one box holds all 128 d); page id of its tile picked in registers
-        constexpr int kPerTile = F8 ? 2 : 4;
-        const int bx = lane * C::kProducers + pw_idx;
-        int my_pg = 0;
-#pragma unroll
-        for (int ti = 0; ti < kWTiles; ++ti) {
-          const int pg = a.paged ? pw.get(i * kWTiles + ti) : 0;
-          if (bx / kPerTile == ti) my_pg = pg;
+        int pg = pg_next;
+        pg_next = page_of(i + 1);
+        const int boxes = min(kWTiles, it.n_tiles - i * kWTiles) * kPerTile;  // with data
+        if (lane == 0) {
+          const int mine = boxes > pw_idx ? (boxes - pw_idx + C::kProducers - 1) / C::kProducers : 0;
+          mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(mine * 2048));
         }
-        // boxes of this warp that hold data (tiles past the chunk end are skipped)
-        int mine = 0;
-        for (int c = pw_idx; c < tiles_here * kPerTile; c += C::kProducers) ++mine;
-        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(mine * 2048));
         __syncwarp();
-        if (lane < C::kBoxesPerWarp && bx < tiles_here * kPerTile) {
-          const int ti = bx / kPerTile;
+        if (bx < boxes) {
+          if (a.paged && (pg < 0 || pg >= a.num_pages)) {
+            if (a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_BAD_PAGE));
+            pg = 0;
+          }
           const int tok = it.t_begin + (i * kWTiles + ti) * kTileTokens;
-          const int grp = a.paged ? my_pg : it.b;
+          const int grp = a.paged ? pg : it.b;
           const int tin = a.paged ? tok % a.page_size : tok;
-          const int half = F8 ? 0 : (bx & 1);
-          const bool is_v = F8 ? (bx & 1) != 0 : (bx & 2) != 0;
-          uint8_t* dst = F8 ? smem + C::kOffLoad + s * C::kLoadBytes +
-                                  (is_v ? kWTiles * kWF8Tile : 0) + ti * kWF8Tile
-                            : smem + C::kOffLoad + s * C::kLoadBytes + (is_v ? 2 * kWHalf : 0) +
-                                  half * kWHalf + ti * 2048;
-          tma_load_4d(dst, is_v ? &v_map : &k_map, &full_bar[s], half * 64, it.kvh, tin, grp,
-                      policy);
+          tma_load_4d(smem + box_off + s * C::kLoadBytes, is_v ? &v_map : &k_map, &full_bar[s],
+                      half * 64, it.kvh, tin, grp, policy);
         }
         __syncwarp();
+        last_g = g;
       }
+      if (!ok) break;
+      gs += it.n_iters;
     }
     cp_async_wait_all();
     if (lane == 0) {
       if (!ok && a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
-      for (int g = max(0, gs - C::kStages); g < gs; ++g)
+      // no copy of this warp may still be landing when the CTA exits
+      for (int g = max(0, last_g - C::kStages + 1); g <= last_g; ++g)
         mbar_wait(&full_bar[g % C::kStages], (g / C::kStages) & 1);
     }
     return;
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         // item idx: (K or V, tile, 8-row block, chunk c, row j); four loads in
         // flight before the conversions
         constexpr int kItems = 2 * kWTiles * 128;
-        constexpr int kCT = 32 * C::kConverters;
+        constexpr int kCT = 32 * (C::kConverters > 0 ? C::kConverters : 1);  // (bf16: unused)
 #pragma unroll
         for (int k0 = 0; k0 < (kItems + kCT - 1) / kCT; k0 += 4) {
           uint4 raw[4];
