@@ -153,7 +153,27 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
     // with the row count (kTokensPerRow tokens per query row at least)
     const int64_t per_cta = ceil_div64(work_tokens * p->num_kv_heads, kRaggedWaves * slots);
     min_chunk = std::max<int64_t>(kMinChunkTokens, static_cast<int64_t>(kTokensPerRow) * rows);
-    const int64_t target = std::max<int64_t>(min_chunk, per_cta);
+    int64_t target = std::max<int64_t>(min_chunk, per_cta);
+    // ... but a small batch keeps at least one chunk per CTA slot: while the
+    // per-row floor leaves fewer chunks than slots, the chunk shrinks (to the
+    // largest length that fills them, not below kMinChunkTokens)
+    auto chunks_of = [&](int64_t c) {
+      int64_t n = 0;
+      for (int32_t b = 0; b < p->batch; ++b) {
+        const int64_t Lb = std::min<int64_t>(std::max(host_seq_lens[b], 0), p->max_seq_len);
+        n += Lb > 0 ? ceil_div64(Lb, c) : 1;
+      }
+      return n * p->num_kv_heads;
+    };
+    if (target > kMinChunkTokens && chunks_of(target) < slots) {
+      int64_t lo = kMinChunkTokens, hi = target;  // chunks_of(hi) < slots
+      while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) / 2;
+        if (chunks_of(mid) >= slots) lo = mid;
+        else hi = mid;
+      }
+      target = lo;
+    }
     splits = ceil_div64(std::max(p->max_seq_len, 1), target);
   }
   splits = std::min<int64_t>(splits, std::max<int64_t>(1, p->max_seq_len / kMinChunkTokens));

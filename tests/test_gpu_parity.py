@@ -188,6 +188,24 @@ def test_wide_schedule_batch_sizes(binding, batch):
         assert np.all(bf16_tensor_to_f64(out)[lens == 0] == 0)
 
 
+def test_plan_small_ragged_batch_fills_the_gpu(binding):
+    """A small ragged batch with wide query groups: the per-row chunk floor (64
+    tokens per query row) would leave far fewer chunks than the tcgen05
+    kernel's CTA slots (one per SM); the planner shrinks the chunk until they
+    fill one wave, and the result still matches the oracle."""
+    shp = W.small_shape("plan_small", batch=2, q_len=8, num_q_heads=64, num_kv_heads=8,
+                        lo=2000, hi=5000, paged=True, causal=True, seed=42)
+    inp = W.make_host_inputs(shp)
+    q, k, v, bt, lens = to_device(inp)
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True)
+    S, chunk = binding.decode_attn_plan(p, inp.seq_lens)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chunks = sum(max(1, -(-int(L) // chunk)) for L in inp.seq_lens) * shp.num_kv_heads
+    assert 256 <= chunk < 64 * 64
+    assert chunks >= sms
+    check(binding, inp, 0)
+    check(binding, inp, S, two_pass=True)
+
 
 # FP8 E4M3 caches (one scale per cache): the narrow kernel widens them to f16
 FP8_CASES = [
