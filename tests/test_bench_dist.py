@@ -49,3 +49,17 @@ def test_single_process_needs_no_process_group(monkeypatch):
     d = bench.Dist()
     assert d.world == 1 and d.rank == 0 and d.pg is None
     assert d.max(4.0) == 4.0
+
+
+def test_oracle_sample_counts_bytes_and_threads():
+    """The CPU baseline's sampler: bytes are whole (request, kv head) units of
+    K+V, and the one-core run reports one thread."""
+    import bench
+    from split_kv_decode_attention_gb300 import workloads as W
+    shp = W.small_shape("cpu_base", batch=2, num_q_heads=4, num_kv_heads=2, lo=50, hi=90, seed=5)
+    inp = W.make_host_inputs(shp)
+    nbytes, secs, threads, note = bench.oracle_sample(inp, 30.0, max_passes=1, threads=1)
+    assert threads == 1 and secs > 0
+    # one full pass: every (request, kv head) unit once, K and V rows of 128 bf16
+    assert nbytes == int(inp.seq_lens.sum()) * shp.num_kv_heads * shp.head_dim * 2 * 2
+    assert note.startswith(f"{shp.batch * shp.num_kv_heads} (request, kv head) units")
