@@ -443,10 +443,11 @@ def run_ours(args, dist: "Dist"):
 
 
 def run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev):
-    """Whole call as a user makes it: copy this step's inputs (q, seq_lens,
-    block table) from pinned host memory, run decode_attn, read out and lse
-    back to the host.  The K/V cache is resident device state, as in a
-    serving engine."""
+    """Whole call as a user makes it, through the C ABI's host-buffer entry:
+    decode_attn_host copies this step's inputs (q, seq_lens, block table) from
+    pinned host memory, runs the kernels, copies out and lse back to pinned
+    host memory and synchronises the stream.  The K/V cache is resident device
+    state, as in a serving engine."""
     import torch
 
     q_h = inp.q.cpu().pin_memory()
@@ -454,24 +455,19 @@ def run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev):
     bt_h = None if inp.block_table is None else inp.block_table.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d = torch.empty_like(inp.q)
-    lens_d = torch.empty_like(inp.seq_lens)
-    bt_d = None if bt_h is None else torch.empty_like(inp.block_table)
+    need = binding.decode_attn_host_workspace_bytes(p, S)
+    ws_h = torch.empty((need + 15) // 16 * 4, dtype=torch.float32, device=dev)
     bi = q_h.numel() * q_h.element_size() + lens_h.numel() * 4 + \
         (0 if bt_h is None else bt_h.numel() * 4)
     bo = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
 
     def one():
-        q_d.copy_(q_h, non_blocking=True)
-        lens_d.copy_(lens_h, non_blocking=True)
-        if bt_d is not None:
-            bt_d.copy_(bt_h, non_blocking=True)
-        binding.decode_attn(q_d, inp.k_cache, inp.v_cache, bt_d, lens_d,
-                            max_seq_len=inp.max_seq_len, num_splits=S, out=out, lse=lse,
-                            workspace=ws, params=p, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        stream.synchronize()
+        _, _, st = binding.decode_attn_host(q_h, inp.k_cache, inp.v_cache, bt_h, lens_h,
+                                            max_seq_len=inp.max_seq_len, num_splits=S,
+                                            out_host=out_h, lse_host=lse_h, workspace=ws_h,
+                                            params=p, stream=stream)
+        if st != 0:
+            raise SystemExit(f"device status {st} in the end-to-end call")
 
     for _ in range(5):
         one()
@@ -484,7 +480,9 @@ def run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev):
     return {"value": round(nbytes["kv"] / med / 1e9, 2), "unit": "GB/s",
             "us_per_call": round(med * 1e6, 2), "h2d_bytes_per_step": int(bi),
             "d2h_bytes_per_step": int(bo), "steps": len(times),
-            "api": "decode_attn (C ABI) with pinned host inputs/outputs; K/V cache resident"}
+            "api": "decode_attn_host (C ABI): q, seq_lens, block table from pinned host memory, "
+                   "out and lse to pinned host memory, copies and stream sync inside the call; "
+                   "K/V cache resident"}
 
 
 # ---------------------------------------------------------------- reference arm

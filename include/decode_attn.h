@@ -270,6 +270,46 @@ int decode_attn_static_workspace(const decode_attn_params *p, const void *q,
                                  void *out, float *lse, int32_t num_splits,
                                  int32_t *status, void *stream);
 
+/*
+ * decode_attn() with the per-call inputs and outputs in host memory: the call
+ * a serving loop makes when q, seq_lens and the block table arrive from the
+ * host and out / lse go back to it, while the K/V cache stays resident on the
+ * device.  One call copies q, seq_lens and the block table into device
+ * staging buffers carved from `workspace`, runs the same kernels as
+ * decode_attn(), copies out and lse (and the status word) back, and returns
+ * once `stream` has finished the call's work.  Unlike every other entry it
+ * synchronises the stream, so it cannot be captured in a CUDA graph.
+ *   q_host            bf16 [B, q_len, Hq, 128] in host memory, dense: the
+ *                     params' q strides must be the packed ones
+ *   k_cache, v_cache  the device caches, as for decode_attn()
+ *   block_table_host  int32 [B, block_table_stride] in host memory, or NULL
+ *                     (contiguous cache)
+ *   seq_lens_host     int32 [B] in host memory
+ *   out_host          bf16 [B, q_len, Hq, 128] in host memory, dense (the
+ *                     params' out strides must be the packed ones)
+ *   lse_host          fp32 [B, q_len, Hq] in host memory
+ *   num_splits        chunks per request; <= 0 asks the planner, which here
+ *                     sees the actual lengths (decode_attn_plan() with
+ *                     seq_lens_host gives the same count, for sizing the
+ *                     workspace)
+ *   workspace         device buffer of >= decode_attn_host_workspace_bytes()
+ *                     bytes for that split count (16-byte aligned): the
+ *                     partials of decode_attn(), then the staging buffers
+ *   status_host       optional int32 host word: the call's DA_STATUS_* bits
+ *   stream            cudaStream_t (NULL: legacy default stream)
+ * Page-locked host buffers (cudaHostAlloc / cudaHostRegister) let the copies
+ * run at full speed; pageable memory works through the driver's staging.
+ * Argument errors return before anything is copied or launched; a failure
+ * after the copies were queued waits for the stream, then returns the code.
+ */
+int decode_attn_host_workspace_bytes(const decode_attn_params *p, int32_t num_splits,
+                                     size_t *bytes);
+int decode_attn_host(const decode_attn_params *p, const void *q_host, const void *k_cache,
+                     const void *v_cache, const int32_t *block_table_host,
+                     const int32_t *seq_lens_host, void *out_host, float *lse_host,
+                     int32_t num_splits, void *workspace, size_t workspace_bytes,
+                     int32_t *status_host, void *stream);
+
 /* Static description of a return code. */
 const char *decode_attn_status_string(int code);
 

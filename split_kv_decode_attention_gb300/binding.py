@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "decode_attn_params_init", "decode_attn_plan", "decode_attn_chunk_len",
     "decode_attn_workspace_bytes", "decode_attn", "decode_attn_split", "decode_attn_combine",
     "decode_attn_status_string", "decode_attn_launch_count", "decode_attn_static_workspace",
+    "decode_attn_host_workspace_bytes", "decode_attn_host",
 )
 DA_ERR_STATIC_WORKSPACE_LIMIT = -11
 STATIC_WORKSPACE_BYTES = 16 << 20
@@ -90,9 +91,12 @@ def lib() -> ctypes.CDLL:
         L.decode_attn_status_string.argtypes = [ctypes.c_int]
         L.decode_attn_status_string.restype = ctypes.c_char_p
         L.decode_attn_launch_count.argtypes = [P, i32]
+        L.decode_attn_host_workspace_bytes.argtypes = [P, i32, ctypes.POINTER(sz)]
+        L.decode_attn_host.argtypes = L.decode_attn.argtypes
         for f in ("decode_attn_plan", "decode_attn_chunk_len", "decode_attn_workspace_bytes",
                   "decode_attn", "decode_attn_split", "decode_attn_combine",
-                  "decode_attn_launch_count", "decode_attn_static_workspace"):
+                  "decode_attn_launch_count", "decode_attn_static_workspace",
+                  "decode_attn_host_workspace_bytes", "decode_attn_host"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -224,6 +228,49 @@ def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
                              int(num_splits), _ptr(workspace) if need > 0 else None, ws_bytes,
                              _ptr(status), _stream_handle(stream)), "decode_attn")
     return out, lse
+
+
+def decode_attn_host_workspace_bytes(p: DecodeAttnParams, num_splits: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().decode_attn_host_workspace_bytes(ctypes.byref(p), int(num_splits),
+                                                  ctypes.byref(n)),
+           "decode_attn_host_workspace_bytes")
+    return n.value
+
+
+def decode_attn_host(q_host, k_cache, v_cache, block_table_host, seq_lens_host, *,
+                     max_seq_len: int, causal: bool = False, scale: Optional[float] = None,
+                     num_splits: int = 0, out_host=None, lse_host=None, workspace=None,
+                     stream=None, params: Optional[DecodeAttnParams] = None,
+                     two_pass: bool = False, k_scale: float = 1.0, v_scale: float = 1.0):
+    """decode_attn with q, block table and seq_lens in host memory (torch CPU
+    tensors, ideally pinned) and out / lse returned to host memory; the K/V
+    cache stays on the device.  One C call: copies in, kernels, copies out,
+    stream synchronised.  Returns (out_host, lse_host, status bits)."""
+    import numpy as np
+    import torch
+
+    B, T, Hq, D = q_host.shape
+    if out_host is None:
+        out_host = torch.empty((B, T, Hq, D), dtype=torch.bfloat16).pin_memory()
+    if lse_host is None:
+        lse_host = torch.empty((B, T, Hq), dtype=torch.float32).pin_memory()
+    p = params if params is not None else params_from_tensors(
+        q_host, k_cache, block_table_host, max_seq_len=max_seq_len, causal=causal, scale=scale,
+        out=out_host, two_pass=two_pass, k_scale=k_scale, v_scale=v_scale)
+    if num_splits <= 0:  # the library's planner, with the actual lengths
+        num_splits, _ = decode_attn_plan(p, np.asarray(seq_lens_host, dtype=np.int32))
+    need = decode_attn_host_workspace_bytes(p, num_splits)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty((need + 15) // 16 * 4, dtype=torch.float32, device=k_cache.device)
+    status = ctypes.c_int32(0)
+    _check(lib().decode_attn_host(ctypes.byref(p), _ptr(q_host), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(block_table_host), _ptr(seq_lens_host), _ptr(out_host),
+                                  _ptr(lse_host), int(num_splits), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
+                                  ctypes.byref(status), _stream_handle(stream)),
+           "decode_attn_host")
+    return out_host, lse_host, status.value
 
 
 def decode_attn_combine(p: DecodeAttnParams, seq_lens, num_splits: int, chunk_len: int,

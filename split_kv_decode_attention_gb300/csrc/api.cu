@@ -489,6 +489,147 @@ int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens, in
   return DA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Staging layout of decode_attn_host's workspace: the partials of
+// decode_attn(), then q, out, lse, seq_lens, the block table and the status
+// word, each at a 256-byte boundary.
+struct HostLayout {
+  size_t part, q, out, lse, lens, bt, status, total;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int host_layout(const decode_attn_params* p, int32_t num_splits, bool paged, HostLayout* h) {
+  size_t part = 0;
+  int rc = decode_attn_workspace_bytes(p, num_splits, &part);
+  if (rc != DA_OK) return rc;
+  const size_t rows = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
+  size_t off = round256(part);
+  h->part = 0;
+  h->q = off;
+  off = round256(off + rows * kHeadDim * 2);
+  h->out = off;
+  off = round256(off + rows * kHeadDim * 2);
+  h->lse = off;
+  off = round256(off + rows * 4);
+  h->lens = off;
+  off = round256(off + static_cast<size_t>(p->batch) * 4);
+  h->bt = off;
+  if (paged) off = round256(off + static_cast<size_t>(p->batch) * p->block_table_stride * 4);
+  h->status = off;
+  h->total = off + 16;
+  return DA_OK;
+}
+
+// Element (b, t, h, d) at ((b * q_len + t) * Hq + h) * 128 + d (strides of
+// dimensions of extent 1 do not matter).
+bool dense_rows(int64_t sb, int64_t st, int64_t sh, const decode_attn_params* p) {
+  const int64_t row = static_cast<int64_t>(p->num_q_heads) * kHeadDim;
+  return (p->num_q_heads == 1 || sh == kHeadDim) && (p->q_len == 1 || st == row) &&
+         (p->batch == 1 || sb == static_cast<int64_t>(p->q_len) * row);
+}
+
+}  // namespace
+
+extern "C" {
+
+int decode_attn_host_workspace_bytes(const decode_attn_params* p, int32_t num_splits,
+                                     size_t* bytes) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (bytes == nullptr) return DA_ERR_NULL_POINTER;
+  HostLayout h;
+  rc = host_layout(p, num_splits, p->page_size > 0, &h);
+  if (rc != DA_OK) return rc;
+  *bytes = h.total;
+  return DA_OK;
+}
+
+int decode_attn_host(const decode_attn_params* p, const void* q_host, const void* k_cache,
+                     const void* v_cache, const int32_t* block_table_host,
+                     const int32_t* seq_lens_host, void* out_host, float* lse_host,
+                     int32_t num_splits, void* workspace, size_t workspace_bytes,
+                     int32_t* status_host, void* stream) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  const bool paged = block_table_host != nullptr;
+  rc = check_paged(p, paged);
+  if (rc != DA_OK) return rc;
+  if (p->batch == 0) {
+    if (status_host != nullptr) *status_host = 0;
+    return DA_OK;
+  }
+  if (q_host == nullptr || seq_lens_host == nullptr || out_host == nullptr ||
+      lse_host == nullptr)
+    return DA_ERR_NULL_POINTER;
+  if (!dense_rows(p->q_stride_batch, p->q_stride_token, p->q_stride_head, p) ||
+      !dense_rows(p->o_stride_batch, p->o_stride_token, p->o_stride_head, p))
+    return DA_ERR_BAD_SHAPE;
+  // the cache checks of decode_attn(), before anything is queued
+  const bool no_keys = p->max_seq_len == 0;
+  if (!no_keys && (k_cache == nullptr || v_cache == nullptr)) return DA_ERR_NULL_POINTER;
+  if (!aligned16(k_cache) || !aligned16(v_cache) ||
+      (!no_keys && (!kv_stride_ok(p, p->kv_stride_page) || !kv_stride_ok(p, p->kv_stride_token) ||
+                    !kv_stride_ok(p, p->kv_stride_head))))
+    return DA_ERR_ALIGNMENT;
+  if (num_splits > 0) {  // the planner below reads the device itself
+    HostLayout h0;
+    rc = host_layout(p, num_splits, paged, &h0);
+    if (rc != DA_OK) return rc;
+    if (workspace == nullptr || workspace_bytes < h0.total || !aligned16(workspace))
+      return DA_ERR_WORKSPACE;
+  }
+  DeviceInfo di;
+  rc = current_device_info(&di);
+  if (rc != DA_OK) return rc;
+  if (di.major * 10 + di.minor < 100) return DA_ERR_NO_DEVICE;
+  if (num_splits <= 0) {
+    int32_t chunk = 0;
+    rc = plan_impl(p, seq_lens_host, &num_splits, &chunk);
+    if (rc != DA_OK) return rc;
+  }
+  HostLayout h;
+  rc = host_layout(p, num_splits, paged, &h);
+  if (rc != DA_OK) return rc;
+  if (workspace == nullptr || workspace_bytes < h.total || !aligned16(workspace))
+    return DA_ERR_WORKSPACE;
+
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
+  const size_t bt_bytes = paged ? static_cast<size_t>(p->batch) * p->block_table_stride * 4 : 0;
+  auto finish = [&](int code) {
+    // the queued copies read or write the caller's host buffers: they must
+    // be done before the call returns, whatever the outcome
+    if (cudaStreamSynchronize(st) != cudaSuccess && code == DA_OK) code = DA_ERR_CUDA;
+    return code;
+  };
+  if (cudaMemcpyAsync(w + h.q, q_host, rows * kHeadDim * 2, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(w + h.lens, seq_lens_host, static_cast<size_t>(p->batch) * 4,
+                      cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      (paged && cudaMemcpyAsync(w + h.bt, block_table_host, bt_bytes, cudaMemcpyHostToDevice,
+                                st) != cudaSuccess) ||
+      cudaMemsetAsync(w + h.status, 0, 4, st) != cudaSuccess)
+    return finish(DA_ERR_CUDA);
+  rc = run_decode(p, w + h.q, k_cache, v_cache,
+                  paged ? reinterpret_cast<const int32_t*>(w + h.bt) : nullptr,
+                  reinterpret_cast<const int32_t*>(w + h.lens), w + h.out,
+                  reinterpret_cast<float*>(w + h.lse), num_splits, w + h.part, h.q,
+                  reinterpret_cast<int32_t*>(w + h.status), stream, true);
+  if (rc != DA_OK) return finish(rc);
+  if (cudaMemcpyAsync(out_host, w + h.out, rows * kHeadDim * 2, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(lse_host, w + h.lse, rows * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      (status_host != nullptr &&
+       cudaMemcpyAsync(status_host, w + h.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess))
+    return finish(DA_ERR_CUDA);
+  return finish(DA_OK);
+}
+
 const char* decode_attn_status_string(int code) {
   switch (code) {
     case DA_OK: return "ok";

@@ -134,6 +134,65 @@ def test_chunk_len_and_workspace_sizes(lib):
         binding.decode_attn_chunk_len(p, 0)
 
 
+def _call_host(lib, p, **kw):
+    a = dict(q=16, k=16, v=16, bt=None, lens=16, out=16, lse=16, splits=1, ws=16,
+             ws_bytes=1 << 30, status=None)
+    a.update(kw)
+    return lib.decode_attn_host(ctypes.byref(p), a["q"], a["k"], a["v"], a["bt"], a["lens"],
+                                a["out"], a["lse"], a["splits"], a["ws"], a["ws_bytes"],
+                                a["status"], None)
+
+
+def test_host_entry_argument_errors(lib):
+    """The host-buffer entry rejects bad arguments before it queues any copy:
+    missing buffers, q / out that are not densely packed, misaligned caches,
+    a workspace smaller than partials plus staging."""
+    p = binding.decode_attn_params_init(2, 1, 8, 2, 128, 0, 0, 0, 64, False)
+    assert _call_host(lib, p, q=None) == -1
+    assert _call_host(lib, p, lse=None) == -1
+    assert _call_host(lib, p, k=None) == -1
+    assert _call_host(lib, p, k=24) == -6
+    need = binding.decode_attn_host_workspace_bytes(p, 1)
+    assert _call_host(lib, p, ws_bytes=need - 1) == -7
+    assert _call_host(lib, p, ws=None) == -7
+    p.q_stride_head = 256                       # heads of q not densely packed
+    assert _call_host(lib, p) == -2
+    p = binding.decode_attn_params_init(2, 3, 8, 2, 128, 0, 0, 0, 64, False)
+    p.o_stride_batch += 128                     # padded batch rows of out
+    assert _call_host(lib, p) == -2
+
+
+def test_host_workspace_holds_partials_and_staging(lib):
+    """decode_attn_host's workspace: decode_attn's partials, then q, out, lse,
+    seq_lens, the block table and the status word at 256-byte boundaries."""
+    p = binding.decode_attn_params_init(3, 2, 8, 2, 128, 16, 100, 500, 1000, True)
+    rows = 3 * 2 * 8
+
+    def r(x):
+        return (x + 255) // 256 * 256
+    off = r(binding.decode_attn_workspace_bytes(p, 7))
+    for size in (rows * 256, rows * 256, rows * 4, 3 * 4, 3 * 100 * 4):
+        off = r(off + size)
+    assert binding.decode_attn_host_workspace_bytes(p, 7) == off + 16
+    p1 = binding.decode_attn_params_init(3, 2, 8, 2, 128, 0, 0, 0, 1000, True)  # contiguous
+    off = r(binding.decode_attn_workspace_bytes(p1, 1))
+    for size in (rows * 256, rows * 256, rows * 4, 3 * 4):
+        off = r(off + size)
+    assert binding.decode_attn_host_workspace_bytes(p1, 1) == off + 16
+
+
+def test_host_entry_empty_batch_and_no_device(lib):
+    p = binding.decode_attn_params_init(0, 1, 8, 2, 128, 0, 0, 0, 64, False)
+    st = ctypes.c_int32(5)
+    assert _call_host(lib, p, q=None, k=None, v=None, lens=None, out=None, lse=None,
+                      ws=None, status=ctypes.byref(st)) == 0
+    assert st.value == 0
+    import torch
+    if not torch.cuda.is_available():
+        p = binding.decode_attn_params_init(1, 1, 8, 2, 128, 0, 0, 0, 64, False)
+        assert _call_host(lib, p) == -9          # checked before any copy is queued
+
+
 def test_status_strings(lib):
     assert binding.decode_attn_status_string(0) == "ok"
     assert "128" in binding.decode_attn_status_string(-3)
