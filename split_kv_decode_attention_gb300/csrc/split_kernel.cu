@@ -623,11 +623,18 @@ constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
 #endif
 constexpr int kF8Stages = DATTN_F8_STAGES;
 constexpr int kF8TilesPerStage = DATTN_F8_TILES_PER_STAGE;
+// Grids of at most one CTA per SM (one short call, e.g. B = 1 at 4K tokens):
+// occupancy no longer hides a CTA's copy latency, so each CTA keeps more
+// bytes in flight -- 3 stages of 4 tiles (96 KB) and four consumer warps
+// (GB300: 17 -> 15 us on B = 1, 32/8 heads, 4096 tokens).
+constexpr int kDeepStages = 3;
+constexpr int kDeepTilesPerStage = 4;
 
-template <int NT, bool CM, bool F8>
+template <int NT, bool CM, bool F8, bool DP = false>
 struct Variant {
-  static constexpr int kSt = F8 ? kF8Stages : kStages;
-  static constexpr int kTps = F8 ? kF8TilesPerStage : kTilesPerStage;
+  static_assert(!(F8 && DP), "the deep shape serves bf16 caches");
+  static constexpr int kSt = F8 ? kF8Stages : DP ? kDeepStages : kStages;
+  static constexpr int kTps = F8 ? kF8TilesPerStage : DP ? kDeepTilesPerStage : kTilesPerStage;
   using C = SplitCfg<NT, kSt, kTps, F8>;
   static constexpr auto kernel = split_kv_kernel<NT, kSt, kTps, CM, F8>;
 };
@@ -635,12 +642,13 @@ struct Variant {
 constexpr int kMaxDev = 64;
 constexpr int kMaxCluster = 16;  // non-portable cluster size limit
 std::mutex g_attr_mu;
-bool g_attr_done[2][2][2][kMaxDev];
-// cached cudaOccupancyMaxActiveClusters per (NT, FP8, cluster size, device); -1 unknown
-int g_max_clusters[2][2][kMaxCluster + 1][kMaxDev];
+bool g_attr_done[2][2][2][2][kMaxDev];
+// cached cudaOccupancyMaxActiveClusters per (NT, FP8, deep, cluster size, device); -1 unknown
+int g_max_clusters[2][2][2][kMaxCluster + 1][kMaxDev];
 bool g_max_clusters_init = false;
+int g_sm_count[kMaxDev];
 
-template <int NT, bool CM, bool F8>
+template <int NT, bool CM, bool F8, bool DP = false>
 cudaError_t ensure_attrs(int* dev_out = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -648,28 +656,42 @@ cudaError_t ensure_attrs(int* dev_out = nullptr) {
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   if (dev_out) *dev_out = dev;
   std::lock_guard<std::mutex> lk(g_attr_mu);
-  if (!g_attr_done[NT - 1][CM][F8][dev]) {
-    e = cudaFuncSetAttribute(Variant<NT, CM, F8>::kernel,
+  if (!g_attr_done[NT - 1][CM][F8][DP][dev]) {
+    e = cudaFuncSetAttribute(Variant<NT, CM, F8, DP>::kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Variant<NT, CM, F8>::C::kSmemBytes);
+                             Variant<NT, CM, F8, DP>::C::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (CM) {
-      e = cudaFuncSetAttribute(Variant<NT, CM, F8>::kernel,
+      e = cudaFuncSetAttribute(Variant<NT, CM, F8, DP>::kernel,
                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
     }
-    g_attr_done[NT - 1][CM][F8][dev] = true;
+    if (g_sm_count[dev] == 0) {
+      e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+    }
+    g_attr_done[NT - 1][CM][F8][DP][dev] = true;
   }
   return cudaSuccess;
 }
 
-template <int NT, bool CM, bool F8>
+// True when a grid of `ctas` CTAs takes the deep shape: bf16 caches and at
+// most one CTA per SM.
+bool deep_grid(bool fp8, int64_t ctas) {
+  if (fp8) return false;
+  int dev = 0;
+  if (ensure_attrs<1, false, false>(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  return ctas <= g_sm_count[dev];
+}
+
+template <int NT, bool CM, bool F8, bool DP>
 void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const SplitArgs& a,
                  cudaStream_t st) {
   cfg = {};
   cfg.gridDim = dim3(a.num_splits, a.num_kv_heads, a.batch);
-  cfg.blockDim = dim3(Variant<NT, CM, F8>::C::kThreads);
-  cfg.dynamicSmemBytes = Variant<NT, CM, F8>::C::kSmemBytes;
+  cfg.blockDim = dim3(Variant<NT, CM, F8, DP>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT, CM, F8, DP>::C::kSmemBytes;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -684,15 +706,15 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const 
   }
 }
 
-template <int NT, bool CM, bool F8>
+template <int NT, bool CM, bool F8, bool DP = false>
 cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitArgs& a,
                       cudaStream_t st) {
-  cudaError_t e = ensure_attrs<NT, CM, F8>();
+  cudaError_t e = ensure_attrs<NT, CM, F8, DP>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  fill_config<NT, CM, F8>(cfg, attr, a, st);
-  return cudaLaunchKernelEx(&cfg, Variant<NT, CM, F8>::kernel, km, vm, a);
+  fill_config<NT, CM, F8, DP>(cfg, attr, a, st);
+  return cudaLaunchKernelEx(&cfg, Variant<NT, CM, F8, DP>::kernel, km, vm, a);
 }
 
 template <int NT, bool F8>
@@ -709,25 +731,27 @@ int ctas_per_sm_nt() {
 }
 
 // How many clusters of `splits` CTAs the device can hold at once.
-template <int NT, bool F8>
+template <int NT, bool F8, bool DP = false>
 int max_active_clusters(int splits) {
   int dev = 0;
-  if (ensure_attrs<NT, true, F8>(&dev) != cudaSuccess) return 0;
+  if (ensure_attrs<NT, true, F8, DP>(&dev) != cudaSuccess) return 0;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (!g_max_clusters_init) {
       for (auto& x : g_max_clusters)
         for (auto& y : x)
           for (auto& z : y)
-            for (int& w : z) w = -1;
+            for (auto& u : z)
+              for (int& w : u) w = -1;
       g_max_clusters_init = true;
     }
-    if (g_max_clusters[NT - 1][F8][splits][dev] >= 0) return g_max_clusters[NT - 1][F8][splits][dev];
+    if (g_max_clusters[NT - 1][F8][DP][splits][dev] >= 0)
+      return g_max_clusters[NT - 1][F8][DP][splits][dev];
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(splits), 1, 1);
-  cfg.blockDim = dim3(Variant<NT, true, F8>::C::kThreads);
-  cfg.dynamicSmemBytes = Variant<NT, true, F8>::C::kSmemBytes;
+  cfg.blockDim = dim3(Variant<NT, true, F8, DP>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT, true, F8, DP>::C::kSmemBytes;
   cudaLaunchAttribute cl[1];
   cl[0].id = cudaLaunchAttributeClusterDimension;
   cl[0].val.clusterDim.x = static_cast<unsigned>(splits);
@@ -736,12 +760,12 @@ int max_active_clusters(int splits) {
   cfg.attrs = cl;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, Variant<NT, true, F8>::kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, Variant<NT, true, F8, DP>::kernel, &cfg) != cudaSuccess) {
     cudaGetLastError();  // clear the (non-sticky) error of a rejected query
     n = 0;
   }
   std::lock_guard<std::mutex> lk(g_attr_mu);
-  g_max_clusters[NT - 1][F8][splits][dev] = n;
+  g_max_clusters[NT - 1][F8][DP][splits][dev] = n;
   return n;
 }
 
@@ -756,6 +780,13 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
                            : launch_nt<1, false, true>(k_map, v_map, a, stream);
     return cluster_merge ? launch_nt<2, true, true>(k_map, v_map, a, stream)
                          : launch_nt<2, false, true>(k_map, v_map, a, stream);
+  }
+  if (deep_grid(false, static_cast<int64_t>(a.num_splits) * a.num_kv_heads * a.batch)) {
+    if (a.rows <= 8)
+      return cluster_merge ? launch_nt<1, true, false, true>(k_map, v_map, a, stream)
+                           : launch_nt<1, false, false, true>(k_map, v_map, a, stream);
+    return cluster_merge ? launch_nt<2, true, false, true>(k_map, v_map, a, stream)
+                         : launch_nt<2, false, false, true>(k_map, v_map, a, stream);
   }
   if (a.rows <= 8)
     return cluster_merge ? launch_nt<1, true, false>(k_map, v_map, a, stream)
@@ -773,10 +804,13 @@ int split_ctas_per_sm(int rows, bool fp8) {
 bool split_cluster_merge_fits(int rows, bool fp8, int num_splits, int64_t num_clusters) {
   if (num_splits < 2 || num_splits > kMaxCluster || num_clusters < 1 || rows > kMaxNarrowRows)
     return false;
+  const bool deep = deep_grid(fp8, num_splits * num_clusters);  // as launch_split decides
   const int n = fp8 ? (rows <= 8 ? max_active_clusters<1, true>(num_splits)
                                  : max_active_clusters<2, true>(num_splits))
-                    : (rows <= 8 ? max_active_clusters<1, false>(num_splits)
-                                 : max_active_clusters<2, false>(num_splits));
+                    : deep ? (rows <= 8 ? max_active_clusters<1, false, true>(num_splits)
+                                        : max_active_clusters<2, false, true>(num_splits))
+                           : (rows <= 8 ? max_active_clusters<1, false>(num_splits)
+                                        : max_active_clusters<2, false>(num_splits));
   // all clusters resident at once: in multi-wave grids the idle CTAs of short
   // requests hold slots (GB300 sweeps: 1.5-2x slower than partials + combine)
   return n >= num_clusters;

@@ -188,6 +188,22 @@ def test_wide_schedule_batch_sizes(binding, batch):
         assert np.all(bf16_tensor_to_f64(out)[lens == 0] == 0)
 
 
+@pytest.mark.parametrize("two_pass", [False, True], ids=["merge-auto", "two-pass"])
+@pytest.mark.parametrize("splits", [1, 3, 7])
+@pytest.mark.parametrize("G,q_len,causal", [(4, 1, False), (4, 4, True), (8, 2, True)],
+                         ids=["rows4", "rows16_causal", "rows16_q2"])
+def test_grids_beyond_one_wave_match_oracle(binding, G, q_len, causal, splits, two_pass):
+    """Grids of more CTAs than SMs run the default pipeline shape (grids of at
+    most one CTA per SM run the deeper one, which the smaller cases cover):
+    40 requests x 4 kv heads x splits CTAs."""
+    shp = W.small_shape("wave", batch=40, q_len=q_len, num_q_heads=4 * G, num_kv_heads=4,
+                        lo=q_len, hi=300, paged=True, causal=causal, seed=50 + G + q_len)
+    inp = W.make_host_inputs(shp)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 40 * 4 * splits > sms
+    check(binding, inp, splits, two_pass=two_pass)
+
+
 def test_plan_small_ragged_batch_fills_the_gpu(binding):
     """A small ragged batch with wide query groups: the per-row chunk floor (64
     tokens per query row) would leave far fewer chunks than the tcgen05
