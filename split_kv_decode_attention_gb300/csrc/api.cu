@@ -28,6 +28,10 @@ constexpr int kMinChunkTokens = 256;
 // (fit on GB300 sweeps of chunk length: ~1-2K tokens for 4-16 rows).
 constexpr int kRaggedWaves = 8;
 constexpr int kTokensPerRow = 64;
+// The tcgen05 kernel (17..128 rows) pays ~3 us per work item (epilogue,
+// the two softmax groups' merge), so its chunks hold twice that (w64: 2
+// chunks of 8K instead of 4 of 4K, ~1.5 % faster).
+constexpr int kWideTokensPerRow = 128;
 // Largest thread-block cluster the split kernel uses (non-portable size).
 constexpr int kMaxClusterSplits = 16;
 
@@ -152,7 +156,8 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
     // costs rows x 516 B of partials written and read back, so chunks grow
     // with the row count (kTokensPerRow tokens per query row at least)
     const int64_t per_cta = ceil_div64(work_tokens * p->num_kv_heads, kRaggedWaves * slots);
-    min_chunk = std::max<int64_t>(kMinChunkTokens, static_cast<int64_t>(kTokensPerRow) * rows);
+    const int per_row = rows > dattn::kMaxNarrowRows ? kWideTokensPerRow : kTokensPerRow;
+    min_chunk = std::max<int64_t>(kMinChunkTokens, static_cast<int64_t>(per_row) * rows);
     int64_t target = std::max<int64_t>(min_chunk, per_cta);
     // ... but a small batch keeps at least one chunk per CTA slot: while the
     // per-row floor leaves fewer chunks than slots, the chunk shrinks (to the
