@@ -55,6 +55,9 @@ namespace {
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
+#ifndef DATTN_Q_SMEM
+#define DATTN_Q_SMEM 1
+#endif
 template <int NT, int STAGES, int TPS, bool F8 = false>
 struct SplitCfg {
   static constexpr int kThreads = 32 * (TPS + 1);        // TPS consumer warps + 1 producer
@@ -72,9 +75,15 @@ struct SplitCfg {
   // warp-merge scratch in the (idle) stage ring, and its per-row LSE
   static constexpr int kXoOffset = (kRedBytes + 127) / 128 * 128;
   static_assert(kXoOffset + kRows * kHeadDim * 4 <= kPipeBytes, "cluster output must fit");
+  // 16-row variants read their Q fragments from shared memory each step
+  // instead of holding all 32 in registers for the whole loop: [16 rows][16
+  // chunks of 16 B], chunk c of row r at c ^ (r & 7) (FP8: d permuted within
+  // each 16-d step to match the K fragments, in f16)
+  static constexpr bool kQSmem = NT == 2 && DATTN_Q_SMEM;
+  static constexpr int kQBytes = kQSmem ? kRows * 256 : 0;
   static constexpr int kBarBytes = 2 * STAGES * 8;
   static constexpr int kStatBytes = 2 * TPS * kRows * 4 + kRows * 4;
-  static constexpr int kSmemBytes = 1024 + kPipeBytes + kBarBytes + kStatBytes;
+  static constexpr int kSmemBytes = 1024 + kPipeBytes + kQBytes + kBarBytes + kStatBytes;
 };
 
 // Byte address of 16-byte chunk `chunk` (0..15, i.e. d = 8*chunk) of token row
@@ -130,7 +139,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
+  uint8_t* q_smem = smem + C::kPipeBytes;  // (16-row variants)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes + C::kQBytes);
   uint64_t* empty_bar = full_bar + STAGES;
   float* stat_m = reinterpret_cast<float*>(empty_bar + STAGES);
   float* stat_l = stat_m + TPS * C::kRows;
@@ -236,27 +246,58 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
   const int g4 = lane >> 2;  // fragment row group
   const int t4 = lane & 3;   // thread in group
   // Q^T as the B operand: rows r = 8*nt + g4, d pairs 2*t4 (+8) of k-step ks
-  uint32_t qf[8][NT][2];
+  // (FP8: 4*t4 and 4*t4 + 2, the d permutation of the FP8 K fragments)
+  auto q_row = [&](int r) -> const uint16_t* {
+    if (r >= a.rows) return nullptr;
+    const int t = r / a.group;
+    const int g = r - t * a.group;
+    return a.q + static_cast<int64_t>(b) * a.q_sb + static_cast<int64_t>(t) * a.q_st +
+           static_cast<int64_t>(kvh * a.group + g) * a.q_sh;
+  };
+  constexpr int kQfSteps = C::kQSmem ? 1 : 8;  // fragments held in registers
+  uint32_t qf[kQfSteps][NT][2];
+  const uint32_t q_lane_addr =
+      smem_addr(q_smem) + ((lane & 7) + 8 * (lane >> 4)) * 256;  // ldmatrix row of this lane
+  if constexpr (C::kQSmem) {
+    // stage the 16 rows once: item (row, 16-d step) per thread
+    for (int idx = threadIdx.x; idx < C::kRows * 8; idx += 32 * TPS) {
+      const int r = idx >> 3, ks = idx & 7;
+      const uint16_t* qr = q_row(r);
+      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+      if (qr != nullptr) {
+        lo = make_uint4(load_u32(qr + 16 * ks), load_u32(qr + 16 * ks + 2),
+                        load_u32(qr + 16 * ks + 4), load_u32(qr + 16 * ks + 6));
+        hi = make_uint4(load_u32(qr + 16 * ks + 8), load_u32(qr + 16 * ks + 10),
+                        load_u32(qr + 16 * ks + 12), load_u32(qr + 16 * ks + 14));
+      }
+      if constexpr (F8) {  // f16; chunk 2ks: d pairs 0,4,8,12; chunk 2ks+1: 2,6,10,14
+        const uint4 c0 = make_uint4(bf16x2_to_f16x2(lo.x), bf16x2_to_f16x2(lo.z),
+                                    bf16x2_to_f16x2(hi.x), bf16x2_to_f16x2(hi.z));
+        const uint4 c1 = make_uint4(bf16x2_to_f16x2(lo.y), bf16x2_to_f16x2(lo.w),
+                                    bf16x2_to_f16x2(hi.y), bf16x2_to_f16x2(hi.w));
+        lo = c0;
+        hi = c1;
+      }
+      *reinterpret_cast<uint4*>(q_smem + r * 256 + (((2 * ks) ^ (r & 7)) << 4)) = lo;
+      *reinterpret_cast<uint4*>(q_smem + r * 256 + (((2 * ks + 1) ^ (r & 7)) << 4)) = hi;
+    }
+    named_barrier_sync(1, 32 * TPS);
+  }
   int lim[NT][2];  // keys j < lim are visible to this thread's two rows
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int r = nt * 8 + g4;
-    const uint16_t* qrow = nullptr;
-    if (r < a.rows) {
-      const int t = r / a.group;
-      const int g = r - t * a.group;
-      qrow = a.q + static_cast<int64_t>(b) * a.q_sb + static_cast<int64_t>(t) * a.q_st +
-             static_cast<int64_t>(kvh * a.group + g) * a.q_sh;
-    }
+    const uint16_t* qrow = q_row(nt * 8 + g4);
+    if constexpr (!C::kQSmem) {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int d = ks * 16 + 2 * t4;
-      qf[ks][nt][0] = qrow ? load_u32(qrow + d) : 0u;
-      qf[ks][nt][1] = qrow ? load_u32(qrow + d + 8) : 0u;
-      if constexpr (F8) {  // the d permutation of the FP8 K fragments
-        const int dp = ks * 16 + 4 * t4;
-        qf[ks][nt][0] = qrow ? bf16x2_to_f16x2(load_u32(qrow + dp)) : 0u;
-        qf[ks][nt][1] = qrow ? bf16x2_to_f16x2(load_u32(qrow + dp + 2)) : 0u;
+      for (int ks = 0; ks < 8; ++ks) {
+        const int d = ks * 16 + 2 * t4;
+        qf[ks][nt][0] = qrow ? load_u32(qrow + d) : 0u;
+        qf[ks][nt][1] = qrow ? load_u32(qrow + d + 8) : 0u;
+        if constexpr (F8) {
+          const int dp = ks * 16 + 4 * t4;
+          qf[ks][nt][0] = qrow ? bf16x2_to_f16x2(load_u32(qrow + dp)) : 0u;
+          qf[ks][nt][1] = qrow ? bf16x2_to_f16x2(load_u32(qrow + dp + 2)) : 0u;
+        }
       }
     }
 #pragma unroll
@@ -299,6 +340,26 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) sc[nt][i] = 0.f;
+      // Q fragments of 16-d step ks: from registers, or (16 rows) one
+      // ldmatrix.x4 from shared memory -- matrices (rows 0-7, chunk 2ks),
+      // (rows 0-7, 2ks + 1), (rows 8-15, 2ks), (rows 8-15, 2ks + 1)
+      auto q_frag = [&](int ks, uint32_t (&f)[NT][2]) {
+        if constexpr (C::kQSmem) {
+          uint32_t r4[4];
+          const int row = (lane & 7) + 8 * (lane >> 4);
+          ldsm_x4(q_lane_addr + (((2 * ks + ((lane >> 3) & 1)) ^ (row & 7)) << 4), r4);
+          f[0][0] = r4[0];
+          f[0][1] = r4[1];
+          f[NT - 1][0] = r4[2];
+          f[NT - 1][1] = r4[3];
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            f[nt][0] = qf[ks % kQfSteps][nt][0];
+            f[nt][1] = qf[ks % kQfSteps][nt][1];
+          }
+        }
+      };
       if constexpr (F8) {
         // FP8 K tile: 16 rows of 128 bytes, 16-byte chunk c of row t at
         // (c ^ (t & 7)); one ldmatrix.x4 covers two 16-d steps
@@ -314,9 +375,10 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
             const uint32_t af[4] = {e4m3x2_to_f16x2(r[2 * h]), e4m3x2_to_f16x2(r[2 * h + 1]),
                                     e4m3x2_to_f16x2(r[2 * h] >> 16),
                                     e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+            uint32_t qb[NT][2];
+            q_frag(2 * kp + h, qb);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma_f16_16816(sc[nt], af, qf[2 * kp + h][nt][0], qf[2 * kp + h][nt][1]);
+            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(sc[nt], af, qb[nt][0], qb[nt][1]);
           }
         }
       } else {
@@ -324,8 +386,10 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         for (int ks = 0; ks < 8; ++ks) {
           uint32_t af[4];
           ldsm_x4(tile_addr(kt, (lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)), af);
+          uint32_t qb[NT][2];
+          q_frag(ks, qb);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], af, qf[ks][nt][0], qf[ks][nt][1]);
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], af, qb[nt][0], qb[nt][1]);
         }
       }
 
@@ -614,9 +678,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
 #endif
 constexpr int kStages = DATTN_STAGES;
 constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
-// FP8 caches: tiles are half the bytes, so the same ring holds more stages
+// FP8 caches: tiles are half the bytes; 4 stages (32 KB) leave room for 5-6
+// CTAs per SM, which the latency-bound 16-row FP8 variant needs (GB300: 4
+// stages 150 us, 6 stages 156 us on 32 requests x q_len 4; B = 1 unchanged)
 #ifndef DATTN_F8_STAGES
-#define DATTN_F8_STAGES 6
+#define DATTN_F8_STAGES 4
 #endif
 #ifndef DATTN_F8_TILES_PER_STAGE
 #define DATTN_F8_TILES_PER_STAGE 2
