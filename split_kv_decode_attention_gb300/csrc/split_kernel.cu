@@ -687,6 +687,12 @@ constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
 #ifndef DATTN_F8_TILES_PER_STAGE
 #define DATTN_F8_TILES_PER_STAGE 2
 #endif
+// the 16-row FP8 variant takes three tiles (three consumer warps) per stage:
+// 12 consumer warps per SM for its latency-bound loop (GB300: 152 -> 136 us
+// on 32 requests x q_len 4; the 8-row variant stays at two, 1 % faster there)
+#ifndef DATTN_F8_NT2_TILES_PER_STAGE
+#define DATTN_F8_NT2_TILES_PER_STAGE 3
+#endif
 constexpr int kF8Stages = DATTN_F8_STAGES;
 constexpr int kF8TilesPerStage = DATTN_F8_TILES_PER_STAGE;
 // Grids of at most one CTA per SM (one short call, e.g. B = 1 at 4K tokens):
@@ -700,7 +706,8 @@ template <int NT, bool CM, bool F8, bool DP = false>
 struct Variant {
   static_assert(!(F8 && DP), "the deep shape serves bf16 caches");
   static constexpr int kSt = F8 ? kF8Stages : DP ? kDeepStages : kStages;
-  static constexpr int kTps = F8 ? kF8TilesPerStage : DP ? kDeepTilesPerStage : kTilesPerStage;
+  static constexpr int kTps = F8 ? (NT == 2 ? DATTN_F8_NT2_TILES_PER_STAGE : kF8TilesPerStage)
+                              : DP ? kDeepTilesPerStage : kTilesPerStage;
   using C = SplitCfg<NT, kSt, kTps, F8>;
   static constexpr auto kernel = split_kv_kernel<NT, kSt, kTps, CM, F8>;
 };
