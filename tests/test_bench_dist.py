@@ -63,3 +63,23 @@ def test_oracle_sample_counts_bytes_and_threads():
     # one full pass: every (request, kv head) unit once, K and V rows of 128 bf16
     assert nbytes == int(inp.seq_lens.sum()) * shp.num_kv_heads * shp.head_dim * 2 * 2
     assert note.startswith(f"{shp.batch * shp.num_kv_heads} (request, kv head) units")
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference runs the fp64 oracle on the host cores (no
+    GPU) and prints one JSON line with the contract's keys."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "0", "--workload", "c1_b1_h32kv8_L4096"],
+                         capture_output=True, text=True, timeout=300, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert (d["n_gpus"], d["steps"], d["warmup"], d["gpu_launches"]) == (1, 2, 0, 0)
+    assert d["higher_is_better"] is True and d["config"]["workload"] == "c1_b1_h32kv8_L4096"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
