@@ -1,7 +1,9 @@
 """Shared helpers of the parity tests: device upload and the tolerance rule.
 
 Tolerance (fixed for this path): bf16 outputs within max-abs 1e-2 and
-mean-abs 1e-3 of the fp64 oracle, fp32 LSE within abs 1e-3.  The max-abs bar
+mean-abs 1e-3 of the fp64 oracle, fp32 LSE within abs 1e-3; the random-shape
+tests also bound the distance in bf16 ulps to the rounded oracle where
+|oracle| >= 0.25.  The max-abs bar
 applies to the computed value before its final rounding to the bf16 output:
 an element may also be off by half a bf16 ulp of the oracle value (the
 output grid), which matters where |oracle| >= 2 (half an ulp there is
@@ -53,6 +55,38 @@ def assert_lse_close(got, ref, what="lse"):
         assert err.max() <= LSE_MAX_ABS, f"{what}: max abs error {err.max():.3e}"
         return float(err.max())
     return 0.0
+
+
+def bf16_rne_bits(x) -> np.ndarray:
+    """bf16 bit patterns of x rounded to nearest even (through fp32)."""
+    f = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((f + 0x7FFF + ((f >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_ulp_distance(a_bits, b_bits) -> np.ndarray:
+    """Number of bf16 values between two bf16 bit patterns (+0 and -0 equal)."""
+    def line(b):
+        b = np.asarray(b).astype(np.int32)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    return np.abs(line(a_bits) - line(b_bits))
+
+
+# Where |oracle| >= ULP_MIN_ABS, the output is within ULP_MAX bf16 ulps of the
+# oracle rounded to bf16 (near zero the ulp shrinks and the absolute bar is
+# the meaningful one)
+ULP_MIN_ABS = 0.25
+ULP_MAX = 2
+
+
+def assert_ulps_close(got_bits, ref, what="out"):
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    d = bf16_ulp_distance(np.asarray(got_bits).ravel(), bf16_rne_bits(ref))
+    sel = np.abs(ref) >= ULP_MIN_ABS
+    if sel.any():
+        worst = int(d[sel].max())
+        assert worst <= ULP_MAX, f"{what}: {worst} bf16 ulps from the rounded oracle"
+        return worst
+    return 0
 
 
 def to_device(inp, device="cuda"):

@@ -9,7 +9,8 @@ import pytest
 
 import oracle
 from split_kv_decode_attention_gb300 import workloads as W
-from tests.parity import assert_lse_close, assert_out_close, bf16_tensor_to_f64, to_device
+from tests.parity import (assert_lse_close, assert_out_close, assert_ulps_close,
+                          bf16_tensor_to_bits, bf16_tensor_to_f64, to_device)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -64,3 +65,4 @@ def test_random_shape_matches_oracle(binding, seed):
     ref_o, ref_l = oracle.decode_attention_inputs(inp)
     assert_out_close(bf16_tensor_to_f64(out), ref_o, what=f"out {shp.name}")
     assert_lse_close(lse.cpu().numpy(), ref_l, what=f"lse {shp.name}")
+    assert_ulps_close(bf16_tensor_to_bits(out), ref_o, what=f"out {shp.name}")
