@@ -11,7 +11,8 @@ import pytest
 
 import oracle
 from split_kv_decode_attention_gb300 import workloads as W
-from tests.parity import assert_lse_close, assert_out_close, bf16_tensor_to_f64
+from tests.parity import (assert_lse_close, assert_out_close, assert_ulps_close,
+                          bf16_tensor_to_bits, bf16_tensor_to_f64)
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -72,3 +73,4 @@ def test_full_size_workload_sampled_rows_match_oracle(binding, name):
     ref_o, ref_l = oracle.decode_attention_inputs(host, rows=rows)
     assert_out_close(o.reshape(-1, 128)[rows], ref_o, what=name)
     assert_lse_close(l.reshape(-1)[rows], ref_l, what=name)
+    assert_ulps_close(bf16_tensor_to_bits(out).reshape(-1, 128)[rows], ref_o, what=name)
