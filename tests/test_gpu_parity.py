@@ -9,8 +9,8 @@ import pytest
 
 import oracle
 from split_kv_decode_attention_gb300 import workloads as W
-from tests.parity import (assert_lse_close, assert_out_close, bf16_tensor_to_bits,
-                          bf16_tensor_to_f64, to_device)
+from tests.parity import (assert_lse_close, assert_out_close, assert_ulps_close,
+                          bf16_tensor_to_bits, bf16_tensor_to_f64, to_device)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -44,6 +44,7 @@ def check(binding, inp, num_splits=0, two_pass=False):
     assert int(status.item()) == 0
     assert_out_close(bf16_tensor_to_f64(out), ref_o)
     assert_lse_close(lse.cpu().numpy(), ref_l)
+    assert_ulps_close(bf16_tensor_to_bits(out), ref_o)
     return out, lse
 
 
