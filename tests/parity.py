@@ -1,10 +1,10 @@
 """Shared helpers of the parity tests: device upload and the tolerance rule.
 
 Tolerance (fixed for this path): bf16 outputs within max-abs 1e-2 and
-mean-abs 1e-3 of the fp64 oracle, fp32 LSE within abs 1e-3; the random-shape
-tests (random, fixed and full-size cases) also bound the distance in bf16 ulps to the rounded oracle where
-|oracle| >= 0.25.  The max-abs bar
-applies to the computed value before its final rounding to the bf16 output:
+mean-abs 1e-3 of the fp64 oracle, fp32 LSE within abs 1e-3; the parity tests
+(fixed, random and full-size cases) also bound the distance in bf16 ulps to
+the rounded oracle where |oracle| >= 0.25.  The max-abs bar applies to the
+computed value before its final rounding to the bf16 output:
 an element may also be off by half a bf16 ulp of the oracle value (the
 output grid), which matters where |oracle| >= 2 (half an ulp there is
 >= 2^-8 ~ 0.0039, and >= 0.0156 from 4 up, coarser than the bar itself).
