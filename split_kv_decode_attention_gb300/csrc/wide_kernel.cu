@@ -395,6 +395,12 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     int gs = 0;       // stages of all previous items
     int last_g = -1;  // the last stage this warp issued
     bool ok = true;
+    // token -> (page, slot): shifts when the page size is a power of two (the
+    // bf16 producers issue 16 boxes a stage and their instruction count sets
+    // the stage pace: w64 226 -> 215 us; the FP8 variant keeps the division)
+    const int ps = a.paged ? a.page_size : 1;
+    const bool ps_pow2 = !F8 && (ps & (ps - 1)) == 0;
+    const int ps_shift = __popc(ps - 1);
     Item it;
     for (int k = 0; ok && schedule_item(sched, a, k, &it); ++k) {
       // ---- this item's query rows into the staging buffer, one row per lane
@@ -422,18 +428,30 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       // tile bx / 4, K or V and the d-half from bx % 4; FP8: tile bx / 2, K or
       // V from bx % 2 (one box holds all 128 d). Each lane loads the page id
       // of its next box a stage ahead and checks it when it is used.
+      // (per-item constants hoisted: the producers' instruction count per
+      // stage sets the stage pace)
       const int32_t* bt_row =
-          a.paged ? a.block_table + static_cast<int64_t>(it.b) * a.bt_stride : nullptr;
+          a.paged && bx < C::kBoxes ? a.block_table + static_cast<int64_t>(it.b) * a.bt_stride
+                                    : nullptr;
+      const int tok_lane = it.t_begin + ti * kTileTokens;  // this lane's tile start, stage 0
+      const int tile_lane_end = it.n_tiles - ti;          // stage i has data if i * kWTiles < this
       auto page_of = [&](int i) -> int {  // raw block-table entry of this lane's tile in stage i
-        const int tile = i * kWTiles + ti;
-        if (bt_row == nullptr || bx >= C::kBoxes || i >= it.n_iters || tile >= it.n_tiles) return 0;
-        return __ldg(bt_row + (it.t_begin + tile * kTileTokens) / a.page_size);
+        if (bt_row == nullptr || i * kWTiles >= tile_lane_end) return 0;
+        const int tok = tok_lane + i * kWTok;
+        return __ldg(bt_row + (ps_pow2 ? tok >> ps_shift : tok / ps));
       };
+      // boxes of this warp in a full stage, and in the item's last one
+      const int last_boxes = (it.n_tiles - (it.n_iters - 1) * kWTiles) * kPerTile;
+      const uint32_t full_bytes =
+          static_cast<uint32_t>((C::kBoxes - pw_idx + C::kProducers - 1) / C::kProducers) * 2048u;
+      const uint32_t last_bytes =
+          static_cast<uint32_t>(last_boxes > pw_idx
+                                    ? (last_boxes - pw_idx + C::kProducers - 1) / C::kProducers
+                                    : 0) * 2048u;
+      int s = gs % C::kStages;         // ring slot and its use count, advanced per stage
+      int use = gs / C::kStages;
       int pg_next = page_of(0);
       for (int i = 0; i < it.n_iters; ++i) {
-        const int g = gs + i;
-        const int s = g % C::kStages;
-        const int use = g / C::kStages;
         int good = 1;
         if (lane == 0 && use > 0) good = mbar_wait_spin(&empty_bar[s], (use - 1) & 1) ? 1 : 0;
         good = __shfl_sync(kFull, good, 0);
@@ -443,25 +461,27 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         }
         int pg = pg_next;
         pg_next = page_of(i + 1);
-        const int boxes = min(kWTiles, it.n_tiles - i * kWTiles) * kPerTile;  // with data
-        if (lane == 0) {
-          const int mine = boxes > pw_idx ? (boxes - pw_idx + C::kProducers - 1) / C::kProducers : 0;
-          mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(mine * 2048));
-        }
+        const bool last = i == it.n_iters - 1;
+        const int boxes = last ? last_boxes : C::kBoxes;  // boxes with data
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], last ? last_bytes : full_bytes);
         __syncwarp();
         if (bx < boxes) {
-          if (a.paged && (pg < 0 || pg >= a.num_pages)) {
+          if (a.paged && static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
             if (a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_BAD_PAGE));
             pg = 0;
           }
-          const int tok = it.t_begin + (i * kWTiles + ti) * kTileTokens;
+          const int tok = tok_lane + i * kWTok;
           const int grp = a.paged ? pg : it.b;
-          const int tin = a.paged ? tok % a.page_size : tok;
+          const int tin = a.paged ? (ps_pow2 ? tok & (ps - 1) : tok % ps) : tok;
           tma_load_4d(smem + box_off + s * C::kLoadBytes, is_v ? &v_map : &k_map, &full_bar[s],
                       half * 64, it.kvh, tin, grp, policy);
         }
         __syncwarp();
-        last_g = g;
+        last_g = gs + i;
+        if (++s == C::kStages) {
+          s = 0;
+          ++use;
+        }
       }
       if (!ok) break;
       gs += it.n_iters;
