@@ -173,6 +173,23 @@ int decode_attn_plan(const decode_attn_params *p, const int32_t *host_seq_lens,
                      int32_t *num_splits, int32_t *chunk_len);
 
 /*
+ * The same planner for an explicit device shape (host only; needs no GPU and
+ * touches no CUDA state), e.g. to plan ahead for another device:
+ *   resident_ctas  CTAs of the split launch resident at once: SMs x CTAs per
+ *                  SM of the kernel this shape runs (decode_attn_plan takes
+ *                  the current device's SM count and the CUDA occupancy of
+ *                  that kernel; on GB300, 152 SMs x 4 for bf16 caches with at
+ *                  most 16 query rows per kv head, x 1 above 16 rows)
+ * Equal lengths (or host_seq_lens NULL): one wave of equal chunks, at most 16
+ * per (request, kv head).  Ragged lengths: chunks for about eight waves of
+ * the real work, at least max(256, 64 x rows) tokens (128 x rows above 16
+ * rows), shrunk (not below 256) while that leaves fewer chunks than resident
+ * CTAs.  Returns DA_ERR_BAD_SHAPE when resident_ctas < 1.
+ */
+int decode_attn_plan_slots(const decode_attn_params *p, const int32_t *host_seq_lens,
+                           int64_t resident_ctas, int32_t *num_splits, int32_t *chunk_len);
+
+/*
  * Chunk length used for a given num_splits: the smallest multiple of 16 that
  * covers max_seq_len in num_splits chunks.  Request b uses
  * ceil(seq_lens[b] / chunk_len) chunks (at least 1).

@@ -30,7 +30,7 @@ DA_FLAG_TEST_WITHHOLD_COPY = 0x100
 DA_ERR_UNSUPPORTED = -12
 
 EXPORTED_SYMBOLS = (
-    "decode_attn_params_init", "decode_attn_plan", "decode_attn_chunk_len",
+    "decode_attn_params_init", "decode_attn_plan", "decode_attn_plan_slots", "decode_attn_chunk_len",
     "decode_attn_workspace_bytes", "decode_attn", "decode_attn_split", "decode_attn_combine",
     "decode_attn_status_string", "decode_attn_launch_count", "decode_attn_static_workspace",
     "decode_attn_host_workspace_bytes", "decode_attn_host",
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
         L.decode_attn_params_init.argtypes = [P] + [i32] * 10
         L.decode_attn_params_init.restype = None
         L.decode_attn_plan.argtypes = [P, vp, pi32, pi32]
+        L.decode_attn_plan_slots.argtypes = [P, vp, ctypes.c_int64, pi32, pi32]
         L.decode_attn_chunk_len.argtypes = [P, i32, pi32]
         L.decode_attn_workspace_bytes.argtypes = [P, i32, ctypes.POINTER(sz)]
         L.decode_attn.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp, vp]
@@ -93,7 +94,8 @@ def lib() -> ctypes.CDLL:
         L.decode_attn_launch_count.argtypes = [P, i32]
         L.decode_attn_host_workspace_bytes.argtypes = [P, i32, ctypes.POINTER(sz)]
         L.decode_attn_host.argtypes = L.decode_attn.argtypes
-        for f in ("decode_attn_plan", "decode_attn_chunk_len", "decode_attn_workspace_bytes",
+        for f in ("decode_attn_plan", "decode_attn_plan_slots", "decode_attn_chunk_len",
+                  "decode_attn_workspace_bytes",
                   "decode_attn", "decode_attn_split", "decode_attn_combine",
                   "decode_attn_launch_count", "decode_attn_static_workspace",
                   "decode_attn_host_workspace_bytes", "decode_attn_host"):
@@ -175,6 +177,20 @@ def decode_attn_plan(p: DecodeAttnParams, host_seq_lens=None) -> Tuple[int, int]
     _check(lib().decode_attn_plan(ctypes.byref(p),
                                   None if arr is None else arr.ctypes.data,
                                   ctypes.byref(ns), ctypes.byref(cl)), "decode_attn_plan")
+    return ns.value, cl.value
+
+
+def decode_attn_plan_slots(p: DecodeAttnParams, host_seq_lens, resident_ctas: int) -> Tuple[int, int]:
+    """The planner for an explicit number of resident split CTAs (host only)."""
+    import numpy as np
+    ns, cl = ctypes.c_int32(), ctypes.c_int32()
+    arr = None
+    if host_seq_lens is not None:
+        arr = np.ascontiguousarray(host_seq_lens, dtype=np.int32)
+    _check(lib().decode_attn_plan_slots(ctypes.byref(p),
+                                        None if arr is None else arr.ctypes.data,
+                                        int(resident_ctas), ctypes.byref(ns), ctypes.byref(cl)),
+           "decode_attn_plan_slots")
     return ns.value, cl.value
 
 

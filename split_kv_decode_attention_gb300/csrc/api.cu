@@ -125,15 +125,13 @@ int chunk_for_splits(const decode_attn_params* p, int32_t num_splits, int32_t* c
   return DA_OK;
 }
 
-int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t* num_splits,
-              int32_t* chunk_len) {
-  DeviceInfo di;
-  int rc = current_device_info(&di);
-  if (rc != DA_OK) return rc;
+// The planner proper: a function of the shape, the host lengths and the
+// number of CTAs the split launch keeps resident at once (SMs x CTAs per SM).
+int plan_for_slots(const decode_attn_params* p, const int32_t* host_seq_lens, int64_t slots,
+                   int32_t* num_splits, int32_t* chunk_len) {
   const int rows = rows_of(p);
   const int64_t max_tiles = ceil_div64(std::max(p->max_seq_len, 1), kTileTokens);
   const int64_t pairs = static_cast<int64_t>(std::max(p->batch, 1)) * p->num_kv_heads;
-  const int64_t slots = static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows, kv_fp8(p));
   bool uniform = true;
   int64_t work_tokens = 0;
   if (host_seq_lens != nullptr) {
@@ -184,11 +182,23 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
   splits = std::min<int64_t>(splits, std::max<int64_t>(1, p->max_seq_len / kMinChunkTokens));
   splits = std::max<int64_t>(1, std::min<int64_t>(splits, max_tiles));
   int32_t chunk = 0, eff = 0;
-  rc = chunk_for_splits(p, static_cast<int32_t>(splits), &chunk, &eff);
+  const int rc = chunk_for_splits(p, static_cast<int32_t>(splits), &chunk, &eff);
   if (rc != DA_OK) return rc;
   *num_splits = eff;
   *chunk_len = chunk;
   return DA_OK;
+}
+
+// The planner on the current device: its SM count times the split launch's
+// resident CTAs per SM for this shape (occupancy of the kernel it will run).
+int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t* num_splits,
+              int32_t* chunk_len) {
+  DeviceInfo di;
+  const int rc = current_device_info(&di);
+  if (rc != DA_OK) return rc;
+  const int64_t slots =
+      static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows_of(p), kv_fp8(p));
+  return plan_for_slots(p, host_seq_lens, slots, num_splits, chunk_len);
 }
 
 int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p, bool paged) {
@@ -275,6 +285,15 @@ int decode_attn_plan(const decode_attn_params* p, const int32_t* host_seq_lens,
   if (rc != DA_OK) return rc;
   if (num_splits == nullptr || chunk_len == nullptr) return DA_ERR_NULL_POINTER;
   return plan_impl(p, host_seq_lens, num_splits, chunk_len);
+}
+
+int decode_attn_plan_slots(const decode_attn_params* p, const int32_t* host_seq_lens,
+                           int64_t resident_ctas, int32_t* num_splits, int32_t* chunk_len) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (num_splits == nullptr || chunk_len == nullptr) return DA_ERR_NULL_POINTER;
+  if (resident_ctas < 1) return DA_ERR_BAD_SHAPE;
+  return plan_for_slots(p, host_seq_lens, resident_ctas, num_splits, chunk_len);
 }
 
 int decode_attn_chunk_len(const decode_attn_params* p, int32_t num_splits, int32_t* chunk_len) {

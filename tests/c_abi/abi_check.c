@@ -1,7 +1,7 @@
 /* A C99 caller of the decode-attention C ABI (host side only): the public
  * header compiles as plain C, and the library linked into a C program gives
- * the documented answers for dense strides, workspace sizes and argument
- * errors without touching a GPU.  Prints "ok" and exits 0, or names the
+ * the documented answers for dense strides, workspace sizes, the planner
+ * for an explicit device shape and argument errors without touching a GPU.  Prints "ok" and exits 0, or names the
  * first failed check and exits 1. */
 #include <stdio.h>
 #include <string.h>
@@ -32,6 +32,17 @@ int main(void) {
         bytes == (size_t)(3 * 2 * 8) * 7 * (128 + 1) * 4);
   CHECK(decode_attn_host_workspace_bytes(&p, 7, &bytes) == DA_OK && bytes > 0);
   CHECK(decode_attn_chunk_len(&p, 0, &chunk) == DA_ERR_SPLITS);
+
+  /* the planner for an explicit device shape: B = 1, 32 heads, 128K tokens
+   * on 152 SMs x 4 resident CTAs -> one wave of 16 chunks of 8192 tokens */
+  {
+    decode_attn_params u;
+    int32_t splits = 0;
+    decode_attn_params_init(&u, 1, 1, 32, 32, DECODE_ATTN_HEAD_DIM, 0, 0, 0, 131072, 0);
+    CHECK(decode_attn_plan_slots(&u, NULL, 152 * 4, &splits, &chunk) == DA_OK && splits == 16 &&
+          chunk == 8192);
+    CHECK(decode_attn_plan_slots(&u, NULL, 0, &splits, &chunk) == DA_ERR_BAD_SHAPE);
+  }
 
   /* argument errors come back before anything is launched */
   CHECK(decode_attn(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, NULL, 0, NULL, NULL) ==
