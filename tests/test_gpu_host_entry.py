@@ -87,3 +87,33 @@ def test_host_entry_reports_device_status(binding):
     _, _, status = binding.decode_attn_host(q_h, k_d, v_d, bt_h, lens_h,
                                             max_seq_len=inp2.max_seq_len, num_splits=1)
     assert status == 0
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[2]], ids=[CASES[0][0], CASES[2][0]])
+def test_host_entry_with_pageable_buffers(binding, case):
+    """Ordinary (pageable) host tensors: the copies go through the driver's
+    staging, and the results are bit-identical to the page-locked call."""
+    name, B, T, Hq, Hkv, lo, hi, paged, causal, fp8 = case
+    shp = W.small_shape(name, batch=B, q_len=T, num_q_heads=Hq, num_kv_heads=Hkv, lo=lo, hi=hi,
+                        paged=paged, causal=causal, seed=80 + B + T, kv_fp8=fp8)
+    inp = W.make_host_inputs(shp)
+    _, k_d, v_d, _, _ = to_device(inp)
+    q_h, bt_h, lens_h = host_tensors(inp)
+    q_p = torch.from_numpy(np.ascontiguousarray(inp.q).view(np.int16)).view(torch.bfloat16)
+    bt_p = None if inp.block_table is None else torch.from_numpy(
+        np.ascontiguousarray(inp.block_table))
+    lens_p = torch.from_numpy(np.ascontiguousarray(inp.seq_lens))
+    out_p = torch.empty((B, T, Hq, 128), dtype=torch.bfloat16)
+    lse_p = torch.empty((B, T, Hq), dtype=torch.float32)
+    assert not q_p.is_pinned() and not out_p.is_pinned() and not lse_p.is_pinned()
+    p = binding.params_from_tensors(q_h, k_d, bt_h, max_seq_len=inp.max_seq_len, causal=causal,
+                                    scale=shp.scale)
+    out_h, lse_h, st_h = binding.decode_attn_host(q_h, k_d, v_d, bt_h, lens_h,
+                                                  max_seq_len=inp.max_seq_len, num_splits=3,
+                                                  params=p)
+    out_p, lse_p, st_p = binding.decode_attn_host(q_p, k_d, v_d, bt_p, lens_p,
+                                                  max_seq_len=inp.max_seq_len, num_splits=3,
+                                                  out_host=out_p, lse_host=lse_p, params=p)
+    assert st_h == 0 and st_p == 0
+    assert np.array_equal(bf16_tensor_to_bits(out_p), bf16_tensor_to_bits(out_h))
+    assert np.array_equal(lse_p.numpy().view(np.uint32), lse_h.numpy().view(np.uint32))
