@@ -38,6 +38,11 @@ MUTANTS = [
     ("length_off_by_one", "int64_t hi = L;\n", "int64_t hi = L - 1;\n"),
     ("causal_off_by_one", "hi = L - J->q_len + 1 + t;", "hi = L - J->q_len + t;"),
     ("causal_tokens_reversed", "hi = L - J->q_len + 1 + t;", "hi = L - t;"),
+    ("key_window_end_ignored", "if (hi > J->key_hi) hi = J->key_hi;", ""),
+    ("key_window_start_ignored", "int64_t lo = J->key_lo > 0 ? J->key_lo : 0;",
+     "int64_t lo = 0;"),
+    ("row_token_index_wrong", "const int t = (int)((flat / Hq) % J->q_len);",
+     "const int t = (int)(flat % J->q_len);"),
     # where the operands come from
     ("gqa_interleaved", "const int kvh = h / G;", "const int kvh = h % J->num_kv_heads;"),
     ("query_token_head_transposed", "(((int64_t)b * J->q_len + t) * Hq + h) * D",
