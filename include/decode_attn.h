@@ -184,7 +184,7 @@ int decode_attn_plan(const decode_attn_params *p, const int32_t *host_seq_lens,
  * per (request, kv head).  Ragged lengths: chunks for about eight waves of
  * the real work, at least max(256, 64 x rows) tokens (128 x rows above 16
  * rows), shrunk (not below 256) while that leaves fewer chunks than resident
- * CTAs.  Returns DA_ERR_BAD_SHAPE when resident_ctas < 1.
+ * CTAs.  Returns DA_ERR_BAD_SHAPE unless 1 <= resident_ctas <= 2^31.
  */
 int decode_attn_plan_slots(const decode_attn_params *p, const int32_t *host_seq_lens,
                            int64_t resident_ctas, int32_t *num_splits, int32_t *chunk_len);

@@ -292,7 +292,7 @@ int decode_attn_plan_slots(const decode_attn_params* p, const int32_t* host_seq_
   int rc = check_shape(p);
   if (rc != DA_OK) return rc;
   if (num_splits == nullptr || chunk_len == nullptr) return DA_ERR_NULL_POINTER;
-  if (resident_ctas < 1) return DA_ERR_BAD_SHAPE;
+  if (resident_ctas < 1 || resident_ctas > (int64_t{1} << 31)) return DA_ERR_BAD_SHAPE;
   return plan_for_slots(p, host_seq_lens, resident_ctas, num_splits, chunk_len);
 }
 

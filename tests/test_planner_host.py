@@ -145,8 +145,14 @@ def test_short_contexts_keep_chunks_of_at_least_256_tokens(max_seq_len, want):
 
 def test_plan_arguments_are_checked():
     p = params(1, 1, 8, 8, 4096, 0)
-    with pytest.raises(binding.DecodeAttnError):
-        binding.decode_attn_plan_slots(p, None, 0)
+    for bad_slots in (0, -5, 2**31 + 1, 2**62):
+        with pytest.raises(binding.DecodeAttnError):
+            binding.decode_attn_plan_slots(p, None, bad_slots)
+    # the largest accepted count plans without overflow (equal and ragged lengths)
+    assert binding.decode_attn_plan_slots(p, None, 2**31)[0] >= 1
+    lens = np.array([100, 4096], np.int32)
+    p2 = params(2, 1, 8, 8, 4096, 16)
+    assert binding.decode_attn_plan_slots(p2, lens, 2**31)[0] >= 1
     bad = params(1, 1, 8, 8, 4096, 0)
     bad.head_dim = 64
     with pytest.raises(binding.DecodeAttnError):
