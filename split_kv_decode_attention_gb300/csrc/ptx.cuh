@@ -215,6 +215,37 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return r;
 }
 
+// Sum of the two values of a packed bf16x2 (or, with f16 = true, f16x2)
+// pair, in fp32 (exact widening).  The probabilities of the P.V product are
+// rounded to 16 bits; normalising the output by the sum of those rounded
+// values (instead of the fp32 ones) makes a row dominated by one key return
+// that key's value row exactly, whatever the rounding of its weight.
+__device__ __forceinline__ float packed_lo(uint32_t v, bool f16) {
+  if (f16) {
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}"
+        : "=f"(r)
+        : "r"(v));
+    return r;
+  }
+  return __uint_as_float(v << 16);
+}
+
+__device__ __forceinline__ float packed_hi(uint32_t v, bool f16) {
+  if (f16) {
+    float r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}"
+        : "=f"(r)
+        : "r"(v));
+    return r;
+  }
+  return __uint_as_float(v & 0xffff0000u);
+}
+
+__device__ __forceinline__ float packed_pair_sum(uint32_t v, bool f16) {
+  return packed_lo(v, f16) + packed_hi(v, f16);
+}
+
 // bf16x2 -> f16x2; exact for magnitudes in f16's normal range [2^-14, 65504].
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));

@@ -82,7 +82,7 @@ struct SplitCfg {
   static constexpr bool kQSmem = NT == 2 && DATTN_Q_SMEM;
   static constexpr int kQBytes = kQSmem ? kRows * 256 : 0;
   static constexpr int kBarBytes = 2 * STAGES * 8;
-  static constexpr int kStatBytes = 2 * TPS * kRows * 4 + kRows * 4;
+  static constexpr int kStatBytes = 3 * TPS * kRows * 4 + kRows * 4;
   static constexpr int kSmemBytes = 1024 + kPipeBytes + kQBytes + kBarBytes + kStatBytes;
 };
 
@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
   uint64_t* empty_bar = full_bar + STAGES;
   float* stat_m = reinterpret_cast<float*>(empty_bar + STAGES);
   float* stat_l = stat_m + TPS * C::kRows;
-  float* xl = stat_l + TPS * C::kRows;  // cluster merge: this CTA's per-row LSE
+  float* stat_q = stat_l + TPS * C::kRows;
+  float* xl = stat_q + TPS * C::kRows;  // cluster merge: this CTA's per-row LSE
 
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -309,13 +310,17 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     }
   }
 
-  float m[NT][2], l[NT][2], acc[8][NT][4];
+  // per row: running max m, the sum l of the fp32 probabilities (the LSE)
+  // and the sum lq of the probabilities as rounded into the P operand (it
+  // normalises O, so the weights P.V applied sum to one exactly)
+  float m[NT][2], l[NT][2], lq[NT][2], acc[8][NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       m[nt][rr] = -INFINITY;
       l[nt][rr] = 0.f;
+      lq[nt][rr] = 0.f;
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -413,6 +418,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
           const float p0 = ex2(x0 - m_use);
           const float p1 = ex2(x1 - m_use);
           l[nt][rr] = l[nt][rr] * alpha + (p0 + p1);
+          lq[nt][rr] *= alpha;
           m[nt][rr] = m_new;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
@@ -428,8 +434,13 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
       uint32_t pb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        pb[nt][0] = movmatrix_trans(F8 ? pack_f16x2(p[nt][0], p[nt][1]) : pack_bf16x2(p[nt][0], p[nt][1]));
-        pb[nt][1] = movmatrix_trans(F8 ? pack_f16x2(p[nt][2], p[nt][3]) : pack_bf16x2(p[nt][2], p[nt][3]));
+        // key j0 (rows rr = 0 low, 1 high), then key j1
+        const uint32_t k0 = F8 ? pack_f16x2(p[nt][0], p[nt][1]) : pack_bf16x2(p[nt][0], p[nt][1]);
+        const uint32_t k1 = F8 ? pack_f16x2(p[nt][2], p[nt][3]) : pack_bf16x2(p[nt][2], p[nt][3]);
+        lq[nt][0] += packed_lo(k0, F8) + packed_lo(k1, F8);
+        lq[nt][1] += packed_hi(k0, F8) + packed_hi(k1, F8);
+        pb[nt][0] = movmatrix_trans(k0);
+        pb[nt][1] = movmatrix_trans(k1);
       }
 
       // ---- keys past seq_len: their V slots may hold anything (NaN * 0 is
@@ -505,6 +516,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
       v += __shfl_xor_sync(kFull, v, 8);
       v += __shfl_xor_sync(kFull, v, 16);
       l[nt][rr] = v;
+      float w = lq[nt][rr];
+      w += __shfl_xor_sync(kFull, w, 4);
+      w += __shfl_xor_sync(kFull, w, 8);
+      w += __shfl_xor_sync(kFull, w, 16);
+      lq[nt][rr] = w;
     }
   if (g4 == 0) {
 #pragma unroll
@@ -514,6 +530,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         const int row = nt * 8 + 2 * t4 + rr;
         stat_m[warp * C::kRows + row] = m[nt][rr];
         stat_l[warp * C::kRows + row] = l[nt][rr];
+        stat_q[warp * C::kRows + row] = lq[nt][rr];
       }
   }
   named_barrier_sync(1, 32 * TPS);
@@ -528,11 +545,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
 #pragma unroll
       for (int w = 0; w < TPS; ++w) M = fmaxf(M, stat_m[w * C::kRows + row]);
       const float Mu = M == -INFINITY ? 0.f : M;
-      float Ls = 0.f;
+      float Qs = 0.f;  // the rounded weights' sum over the warps
 #pragma unroll
       for (int w = 0; w < TPS; ++w)
-        Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
-      const float f = (Ls > 0.f ? ex2(m[nt][rr] - Mu) / Ls : 0.f) * (F8 ? a.v_scale : 1.f);
+        Qs += stat_q[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
+      const float f = (Qs > 0.f ? ex2(m[nt][rr] - Mu) / Qs : 0.f) * (F8 ? a.v_scale : 1.f);
       // accumulator rows g4 / g4 + 8 of output tile mt hold d = 16mt + g4 /
       // + 8 (bf16 path) or d = 16mt + 2g4 / + 1 (FP8 path)
       float* dst = red + (warp * C::kRows + row) * C::kRedStride + (F8 ? 2 * g4 : g4);

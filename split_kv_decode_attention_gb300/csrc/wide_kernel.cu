@@ -76,8 +76,10 @@ constexpr int kWF8Tile = kTileTokens * 128;  // one FP8 tile (K or V): 16 rows o
 // CTA), and up to which the partial chunks are sorted by length.
 constexpr int kWMaxSchedBatch = 1024;
 constexpr int kWSortBatch = 256;
-constexpr int kWStatFloats = 4 * kWRows + 2;       // m, l per group and row; ok per group
-constexpr int kWStatBytes = 2560;
+// m, l (fp32 probabilities: the LSE) and lq (the same probabilities rounded
+// to the 16-bit P operand: normalises O) per group and row; ok per group
+constexpr int kWStatFloats = 6 * kWRows + 2;
+constexpr int kWStatBytes = 3200;
 constexpr int kWSchedInts = 4 * kWMaxSchedBatch + 4;
 static_assert(kWStatFloats * 4 <= kWStatBytes, "statistics buffer");
 
@@ -724,7 +726,8 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     }
 
     float m_used = -INFINITY;  // reference max of P (log2 domain), raised lazily
-    float l = 0.f;
+    float l = 0.f;             // sum of the fp32 probabilities (for the LSE)
+    float lq = 0.f;            // sum of the probabilities as rounded into P (divides O)
     const int n_iters = it.n_iters;
     const int my_tiles = grp == 0 ? (n_iters + 1) >> 1 : n_iters >> 1;
     for (int j = grp; ok && j < n_iters; j += 2) {
@@ -771,15 +774,17 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       if (raise) m_used = mt;
       const float mref = m_used == -INFINITY ? 0.f : m_used;  // all masked so far: p = 0
       uint32_t pk[kWTok / 2];
-      float psum = 0.f;
+      float psum = 0.f, qsum = 0.f;
 #pragma unroll
       for (int i = 0; i < kWTok; i += 2) {
         const float p0 = ex2(x[i] - mref);
         const float p1 = ex2(x[i + 1] - mref);
         psum += p0 + p1;
         pk[i / 2] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        qsum += packed_pair_sum(pk[i / 2], F8);
       }
       l = l * alpha + psum;
+      lq = lq * alpha + qsum;
 
       // ---- this group's previous P.V (tile j - 2) must be done before its O
       // is rescaled and its P buffer rewritten (the previous use may belong to
@@ -839,20 +844,22 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     float* stat = reinterpret_cast<float*>(smem + C::kOffStat + (k & 1) * kWStatBytes);
     tc_fence_before_sync();
     named_barrier_sync(4, kWSoftmaxThreads);  // both groups' last P.V are done
-    stat[grp * 256 + r] = m_used;
-    stat[grp * 256 + 128 + r] = l;
-    if (tid == grp * 128) stat[512 + grp] = ok ? 1.f : 0.f;
+    stat[grp * 384 + r] = m_used;
+    stat[grp * 384 + 128 + r] = l;
+    stat[grp * 384 + 256 + r] = lq;
+    if (tid == grp * 128) stat[768 + grp] = ok ? 1.f : 0.f;
     named_barrier_sync(4, kWSoftmaxThreads);
     tc_fence_after_sync();
-    ok = stat[512] != 0.f && stat[513] != 0.f;  // the same for all 256 threads
-    const float m0 = stat[r], l0 = stat[128 + r];
-    const float m1 = stat[256 + r], l1 = stat[384 + r];
+    ok = stat[768] != 0.f && stat[769] != 0.f;  // the same for all 256 threads
+    const float m0 = stat[r], l0 = stat[128 + r], q0 = stat[256 + r];
+    const float m1 = stat[384 + r], l1 = stat[512 + r], q1 = stat[640 + r];
     const float M = fmaxf(m0, m1);
     const float Mu = M == -INFINITY ? 0.f : M;
     const float f0 = l0 > 0.f ? ex2(m0 - Mu) : 0.f;
     const float f1 = l1 > 0.f ? ex2(m1 - Mu) : 0.f;
-    const float Lt = l0 * f0 + l1 * f1;
-    const float inv = (Lt > 0.f ? 1.f / Lt : 0.f) * (F8 ? a.v_scale : 1.f);
+    const float Lt = l0 * f0 + l1 * f1;  // the LSE's sum
+    const float Qt = q0 * f0 + q1 * f1;  // the weights P.V actually used
+    const float inv = (Qt > 0.f ? 1.f / Qt : 0.f) * (F8 ? a.v_scale : 1.f);
     const bool have0 = ok && n_iters > 0;  // O[0] / O[1] were written
     const bool have1 = ok && n_iters > 1;
     const bool direct = it.nsplit == 1;

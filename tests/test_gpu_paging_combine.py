@@ -1,5 +1,7 @@
 """GPU checks of the paged gather, the split partials, the combine step, the
 device status word and CUDA-graph capture.  All calls go through the C ABI."""
+import zlib
+
 import numpy as np
 import pytest
 
@@ -76,6 +78,60 @@ def test_shuffled_pages_bit_identical_to_contiguous(binding, page_size, splits):
     assert np.array_equal(bf16_tensor_to_bits(o1), bf16_tensor_to_bits(o2))
     assert np.array_equal(l1.cpu().numpy().view(np.uint32), l2.cpu().numpy().view(np.uint32))
     ref_o, ref_l = oracle.decode_attention(q, kc, vc, lens, num_kv_heads=Hkv)
+    assert_out_close(bf16_tensor_to_f64(o2), ref_o)
+    assert_lse_close(l2.cpu().numpy(), ref_l)
+
+
+# Every kernel variant and merge path: (rows per KV head via heads x q_len,
+# causal), splits, flags.  4 rows: the 8-row warp-MMA kernel; 16 rows (GQA 4
+# x 4 causal tokens): the 16-row variant with Q in shared memory; 64 and 128
+# rows: the tcgen05 kernel.  "merge" lets decode_attn pick the cluster merge
+# where it applies; "two-pass" forces partials in the workspace + combine.
+PAGING_VARIANTS = [
+    # id, Hq, Hkv, q_len, causal, splits, two_pass
+    ("rows4_direct", 8, 2, 1, False, 1, False),
+    ("rows4_two_pass", 8, 2, 1, False, 3, True),
+    ("rows16_merge", 8, 2, 4, True, 3, False),
+    ("rows16_two_pass", 8, 2, 4, True, 5, True),
+    ("rows64_tcgen05_direct", 16, 2, 8, True, 1, False),
+    ("rows64_tcgen05_two_pass", 16, 2, 8, True, 3, True),
+    ("rows128_tcgen05_two_pass", 16, 1, 8, True, 2, True),
+]
+
+
+@pytest.mark.parametrize("kv_fp8", [False, True], ids=["bf16", "fp8"])
+@pytest.mark.parametrize("variant", PAGING_VARIANTS, ids=[v[0] for v in PAGING_VARIANTS])
+def test_every_kernel_path_bit_identical_paged_vs_contiguous(binding, variant, kv_fp8):
+    """The same logical K/V stored contiguously and as shuffled 16-token
+    pages give identical bits out (out and LSE) on every kernel variant and
+    merge path, bf16 and FP8 caches: the gather maps logical positions
+    exactly, and no reduction order depends on the physical layout."""
+    name, Hq, Hkv, T, causal, splits, two_pass = variant
+    rng = np.random.default_rng(zlib.crc32(name.encode()) + int(kv_fp8))
+    B, Lmax, D = 5, 1100, 128
+    x = lambda: rng.standard_normal((B, Lmax, Hkv, D), dtype=np.float32)  # noqa: E731
+    if kv_fp8:
+        (kc, ks), (vc, vs) = W.quantize_e4m3(x()), W.quantize_e4m3(x())
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    else:
+        kc, vc, ks, vs = W.f32_to_bf16_bits(x()), W.f32_to_bf16_bits(x()), 1.0, 1.0
+        dev = bf
+    q = W.f32_to_bf16_bits(rng.standard_normal((B, T, Hq, D), dtype=np.float32))
+    lens = np.array([1100, T, 333, 16 + T, 777], np.int32)
+    kp, vp, bt = paginate(kc, vc, lens, 16, rng)
+    lens_d = torch.from_numpy(lens).cuda()
+    kw = dict(max_seq_len=Lmax, num_splits=splits, causal=causal, two_pass=two_pass,
+              k_scale=ks, v_scale=vs)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1, l1 = binding.decode_attn(bf(q), dev(kc), dev(vc), None, lens_d, status=status, **kw)
+    o2, l2 = binding.decode_attn(bf(q), dev(kp), dev(vp), torch.from_numpy(bt).cuda(), lens_d,
+                                 status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(bf16_tensor_to_bits(o1), bf16_tensor_to_bits(o2))
+    assert np.array_equal(l1.cpu().numpy().view(np.uint32), l2.cpu().numpy().view(np.uint32))
+    ref_o, ref_l = oracle.decode_attention(q, kc, vc, lens, num_kv_heads=Hkv, causal=causal,
+                                           kv_fp8=kv_fp8, k_scale=ks, v_scale=vs)
     assert_out_close(bf16_tensor_to_f64(o2), ref_o)
     assert_lse_close(l2.cpu().numpy(), ref_l)
 

@@ -33,3 +33,12 @@ def test_ulps_check_ignores_small_values_and_flags_large_ones():
         raise RuntimeError("not flagged")
     except AssertionError:
         pass
+
+
+def test_output_tolerance_widens_only_from_four():
+    """The max-abs bar is 1e-2 flat below |oracle| = 4 and 1e-2 plus half a
+    bf16 ulp (2^-6 on [4, 8)) from there up."""
+    from tests.parity import out_tolerance
+    tol = out_tolerance(np.array([0.0, 1.5, 2.5, -3.99, 4.0, -5.0, 9.0]))
+    assert np.array_equal(tol[:4], np.full(4, 1e-2))
+    assert np.allclose(tol[4:], [1e-2 + 2.0 ** -6, 1e-2 + 2.0 ** -6, 1e-2 + 2.0 ** -5])
