@@ -277,8 +277,13 @@ int decode_attn_combine(const decode_attn_params *p, const int32_t *seq_lens,
  *   - All calls on a device share the array, and it keeps the last call's
  *     contents (nothing in it needs clearing).  Calls that overlap on the GPU
  *     race on it: serialise them.
- *   - The first call on each device looks up the array's address with that
- *     device current; make it before any stream capture on that device.
+ *   - The first call in each CUDA context looks up the array's address with
+ *     that device current (once per device; again after cudaDeviceReset, or
+ *     in another context a driver-API caller made current); make it before
+ *     any stream capture in that context.
+ *   - Only calls that write partials (decode_attn_launch_count() == 2) use
+ *     the array and count against the limit; single-chunk and cluster-merged
+ *     calls never do.
  * Allocates nothing (no cudaMalloc/cudaFree or allocating library call).
  */
 int decode_attn_static_workspace(const decode_attn_params *p, const void *q,
