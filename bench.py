@@ -2,7 +2,11 @@
 
 One step = one decode-attention call (split kernel + combine kernel when a
 request spans several chunks) over one batch of synthetic, HBM-resident
-inputs.  Prints ONE JSON line (rank 0):
+inputs.  The default run times the five gate workloads one after another
+(c1..c5, each with the same --steps / --warmup); the headline is the largest
+single-GPU one, c3 (64 ragged paged requests, 4.4 GB of K/V), and
+`per_config` carries the same figures for c1, c2, c4 and c5.  `--workload`
+names one workload instead.  Prints ONE JSON line (rank 0):
 
   value        KV-read GB/s = algorithmic K+V bytes / device time per call
   ms_per_step  device time per call (CUDA events on the launching stream)
@@ -40,9 +44,15 @@ from split_kv_decode_attention_gb300 import workloads as W  # noqa: E402
 
 METRIC = ("split-KV decode attention: KV-read HBM GB/s (% of GB300 peak), "
           "μs per call")
-DEFAULT_WORKLOAD = "c2_b1_mha32_L131072"
+GATE_WORKLOADS = ["c1_b1_h32kv8_L4096", "c2_b1_mha32_L131072",
+                  "c3_b64_h32kv8_L512-32768_paged",
+                  "c4_b256_h64kv8_L128-4096_paged_peaked",
+                  "c5_b32_q4_causal_h32kv8_L1024-16384_paged"]
+HEADLINE_WORKLOAD = "c3_b64_h32kv8_L512-32768_paged"
+DEFAULT_WORKLOAD = "gate"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal (context; the roofline uses the measured copy)
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 # the kernel that reads K/V, by rows per KV head (q_len x heads per KV head),
 # and the sources its machine code depends on (a committed ncu summary is
@@ -65,13 +75,16 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[DEFAULT_WORKLOAD] + list(W.WORKLOADS),
+                    help="'gate': c1..c5 with the headline on c3; or one workload")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="chunks per request (0: the library's planner)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="wall-clock budget of the CPU-baseline sample")
+                    help="wall-clock budget of the headline's CPU-baseline sample "
+                         "(the other gate workloads get a third of it)")
     return ap.parse_args(argv)
 
 
@@ -110,7 +123,8 @@ def profiled_traffic(workload: str, kernel: str = "split_kv_kernel"):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled in the background."""
+    """nvidia-smi clocks / throttle reasons sampled in the background for the
+    whole run; summary(t0, t1) describes the samples inside one timed window."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -120,7 +134,6 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.lines = []
-        self.mark = None
 
     def start(self):
         try:
@@ -138,21 +151,12 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.perf_counter(), line.strip()))
 
-    def window(self, t0, t1):
-        self.mark = (t0, t1)
-
-    def stop(self):
+    def summary(self, t0, t1):
         if self.proc is None:
             return None
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
         rows = []
-        for ts, line in self.lines:
-            if self.mark and not (self.mark[0] - 0.15 <= ts <= self.mark[1] + 0.15):
+        for ts, line in list(self.lines):
+            if not (t0 - 0.15 <= ts <= t1 + 0.15):
                 continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
@@ -172,6 +176,16 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[0] for r in rows),
                 "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": sorted(seen), "samples": len(rows)}
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
 
 
 # ---------------------------------------------------------------- distributed
@@ -273,20 +287,15 @@ def host_copy(inp_dev):
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, dist: "Dist"):
+def measure(args, dist: "Dist", binding, name: str, dev, clocks: "ClockSampler",
+            cpu_budget: float):
+    """Time one workload: K calls (split + combine launches, exactly what
+    decode_attn makes) bracketed by CUDA events on the launching stream after
+    W warm-up calls, plus the informational single-call, warm-L2 and
+    end-to-end figures and the CPU oracle's sample.  Returns a dict."""
     import torch
-    from split_kv_decode_attention_gb300 import binding
-    from split_kv_decode_attention_gb300 import build as cuda_build
 
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA GPU")
-    dev = torch.device("cuda", dist.local)
-    torch.cuda.set_device(dev)
-    if not os.path.exists(binding.LIB_PATH):
-        cuda_build.build()
-    binding.lib()
-
-    shape = W.WORKLOADS[args.workload]
+    shape = W.WORKLOADS[name]
     inp = W.make_device_inputs(shape, device=str(dev))
     lens_h = inp.seq_lens.cpu().numpy()
     nbytes = algorithmic_bytes(shape, lens_h)
@@ -311,6 +320,8 @@ def run_ours(args, dist: "Dist"):
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
 
     def step(e0=None, e1=None, e2=None):
+        # e1 splits the split kernel from the combine; with one launch there is
+        # nothing between them and the call ends at e1 (no empty event pair)
         if e0 is not None:
             e0.record(stream)
         binding.decode_attn_split(p, q, k, v, bt, lens, out, lse, S, workspace=ws,
@@ -319,8 +330,8 @@ def run_ours(args, dist: "Dist"):
             e1.record(stream)
         if launches > 1:
             binding.decode_attn_combine(p, lens, S, chunk, ws, out, lse, stream=stream)
-        if e2 is not None:
-            e2.record(stream)
+            if e2 is not None:
+                e2.record(stream)
 
     for _ in range(max(args.warmup, 3)):
         if flush:
@@ -329,9 +340,6 @@ def run_ours(args, dist: "Dist"):
     torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    clocks.start()
-    time.sleep(0.3)
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -342,14 +350,13 @@ def run_ours(args, dist: "Dist"):
     torch.cuda.synchronize()
     dist.barrier()
     t1 = time.perf_counter()
-    clocks.window(t0, t1)
-    clk = clocks.stop()
+    clk = clocks.summary(t0, t1)
     split_ms = np.array([a.elapsed_time(b) for a, b, _ in ev])
-    call_ms = np.array([a.elapsed_time(c) for a, _, c in ev])
+    call_ms = np.array([a.elapsed_time(c if launches > 1 else b) for a, b, c in ev])
     comb_ms = call_ms - split_ms
     st = int(status.item())
     if st != 0:
-        raise SystemExit(f"device status {st} during the bench")
+        raise SystemExit(f"{name}: device status {st} during the bench")
 
     ms = float(call_ms.mean())
     ms_all = dist.max(ms, dev)
@@ -358,7 +365,7 @@ def run_ours(args, dist: "Dist"):
     split_mean_ms = float(split_ms.mean())
     achieved = nbytes["total"] / (split_mean_ms * 1e-3) / 1e9
     kernel = dominant_kernel(shape)
-    traffic = profiled_traffic(args.workload, kernel)
+    traffic = profiled_traffic(name, kernel)
 
     # informational, outside the timed steps: the same call as one
     # decode_attn() with no event between the two launches, so the combine
@@ -376,6 +383,33 @@ def run_ours(args, dist: "Dist"):
         fused.append((a_ev, b_ev))
     torch.cuda.synchronize()
     fused_us = float(np.median([a.elapsed_time(b) for a, b in fused])) * 1e3
+
+    # informational, outside the timed steps: the graph-capturable default
+    # call, decode_attn(num_splits=0), which plans on the device from the
+    # lengths in device memory (two or more requests: planner kernel, split,
+    # combine) -- the call a serving loop with device-side seq_lens makes
+    ws_auto = torch.empty((binding.decode_attn_workspace_bytes(p, 0) + 3) // 4 + 1,
+                          dtype=torch.float32, device=dev)
+    auto_launches = binding.decode_attn_launch_count(p, 0)
+    auto = []
+    for i in range(min(args.steps, 200) + 3):
+        if flush:
+            flush_buf.fill_(1)
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len, num_splits=0,
+                            out=out, lse=lse, workspace=ws_auto, status=status, params=p,
+                            stream=stream)
+        b_ev.record(stream)
+        if i >= 3:
+            auto.append((a_ev, b_ev))
+    torch.cuda.synchronize()
+    auto_us = float(np.median([a.elapsed_time(b) for a, b in auto])) * 1e3
+    auto_plan = {"us_per_call": round(auto_us, 2), "launches": auto_launches,
+                 "vs_host_length_plan": round(auto_us / fused_us, 4),
+                 "note": "decode_attn(num_splits=0): planned on the device from seq_lens "
+                         "(one request: host plan); median of calls, informational"}
+    del ws_auto
 
     # informational, outside the timed steps: with a flushed workload (K/V
     # smaller than 4x L2), the same call again with K/V left warm in L2
@@ -397,29 +431,28 @@ def run_ours(args, dist: "Dist"):
     e2e = run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev)
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
-        hb, secs, threads, note = oracle_sample(host_copy(inp), args.cpu_seconds)
+        host = host_copy(inp)
+        hb, secs, threads, note = oracle_sample(host, cpu_budget)
         cpu = {"value": hb / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": note + f"; {secs:.1f} s of oracle time"}
         # the same oracle on one host core, over a shorter budget
-        hb1, secs1, _, note1 = oracle_sample(host_copy(inp), args.cpu_seconds / 4, threads=1)
+        hb1, secs1, _, note1 = oracle_sample(host, cpu_budget / 4, threads=1)
+        del host
         cpu["one_core"] = {"value": hb1 / secs1 / 1e9, "unit": "GB/s", "cores": 1,
                            "sample": note1 + f"; {secs1:.1f} s of oracle time"}
-    if dist.rank != 0:
-        dist.close()
-        return None
     res = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
-        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_all, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16 (FP8 E4M3 K/V widened)" if shape.kv_fp8 else "bf16",
-        "data": "synthetic",
+        "value": round(value, 2), "unit": "GB/s",
+        "ms_per_step": round(ms_all, 6),
         "us_per_call": round(ms_all * 1e3, 2),
         "us_per_call_median": round(float(np.median(call_ms)) * 1e3, 2),
         "us_per_call_p10_p90": [round(float(np.percentile(call_ms, 10)) * 1e3, 2),
                                 round(float(np.percentile(call_ms, 90)) * 1e3, 2)],
         "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
+        "pct_of_nominal_hbm_peak": round(100 * value / dist.world / NOMINAL_HBM_GBS, 2),
         "us_per_call_single_decode_attn": round(fused_us, 2),
-        "config": {"workload": args.workload, "kv_dtype": "fp8_e4m3" if shape.kv_fp8 else "bf16",
+        "auto_plan": auto_plan,
+        "dtype": "f16 (FP8 E4M3 K/V widened)" if shape.kv_fp8 else "bf16",
+        "config": {"workload": name, "kv_dtype": "fp8_e4m3" if shape.kv_fp8 else "bf16",
                    "batch": shape.batch, "q_len": shape.q_len,
                    "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
                    "head_dim": shape.head_dim, "seq_lens": [int(lens_h.min()), int(lens_h.max())],
@@ -438,6 +471,54 @@ def run_ours(args, dist: "Dist"):
         "e2e": e2e, "gpu_launches": args.steps * launches, "clocks": clk,
         "cpu_baseline": cpu,
     }
+    del inp, q, k, v, bt, lens, out, lse, ws, flush_buf
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, dist: "Dist"):
+    import torch
+    from split_kv_decode_attention_gb300 import binding
+    from split_kv_decode_attention_gb300 import build as cuda_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    if not os.path.exists(binding.LIB_PATH):
+        cuda_build.build()
+    binding.lib()
+
+    gate = args.workload == DEFAULT_WORKLOAD
+    names = GATE_WORKLOADS if gate else [args.workload]
+    head = HEADLINE_WORKLOAD if gate else args.workload
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    per = {}
+    try:
+        for name in names:
+            budget = args.cpu_seconds if name == head else args.cpu_seconds / 3
+            per[name] = measure(args, dist, binding, name, dev, clocks, budget)
+    finally:
+        clocks.stop()
+    if dist.rank != 0:
+        dist.close()
+        return None
+    h = per.pop(head)
+    res = {
+        "metric": METRIC, "value": h["value"], "unit": "GB/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": h["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": h["dtype"], "data": "synthetic",
+    }
+    res.update({k: v for k, v in h.items() if k not in res})
+    if per:
+        res["per_config"] = per
+        res["headline_note"] = (
+            "value, roofline, e2e and cpu_baseline are for c3 (largest single-GPU gate "
+            "workload); per_config has the same keys for c1, c2, c4, c5, each timed with the "
+            "same --steps/--warmup")
     dist.close()
     return res
 
@@ -492,7 +573,8 @@ def run_reference(args):
     window sized so the whole run stays within a few minutes."""
     import oracle
 
-    shape = W.WORKLOADS[args.workload]
+    name = HEADLINE_WORKLOAD if args.workload == DEFAULT_WORKLOAD else args.workload
+    shape = W.WORKLOADS[name]
     inp = W.make_host_inputs(shape)
     oracle.build()
     threads = oracle.default_threads()
@@ -532,7 +614,7 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "batch": shape.batch,
+        "config": {"workload": name, "batch": shape.batch,
                    "num_q_heads": shape.num_q_heads, "num_kv_heads": shape.num_kv_heads,
                    "q_len": shape.q_len, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,

@@ -205,6 +205,9 @@ int decode_attn_chunk_len(const decode_attn_params *p, int32_t num_splits,
  * a row is normalised (sum of weights 1) over its chunk's keys; an empty
  * chunk has lse -inf.  Entries of requests that use a single chunk are not
  * written.
+ * num_splits <= 0: the need of the planned call -- for a device-planned call
+ * (see "Device planning" at decode_attn) a bound that does not depend on the
+ * lengths, for one request the host plan's need.  Reads the current device.
  */
 int decode_attn_workspace_bytes(const decode_attn_params *p, int32_t num_splits,
                                 size_t *bytes);
@@ -225,6 +228,25 @@ int decode_attn_workspace_bytes(const decode_attn_params *p, int32_t num_splits,
  *   status       optional int32 device word; DA_STATUS_* bits are OR-ed in
  *   stream       cudaStream_t to launch on (NULL: legacy default stream)
  * Device pointers only.  Asynchronous with respect to the host.
+ *
+ * Device planning (num_splits <= 0 with two or more requests; for the
+ * tcgen05 kernel, above 16 rows per kv head, at most 1024 requests).  The
+ * lengths may exist only on the device -- and change between replays of a
+ * captured graph -- so the call plans there: a one-CTA planner kernel applies
+ * decode_attn_plan()'s rule to the current seq_lens (the same plan the host
+ * planner gives for those lengths), then the split kernel runs one CTA per
+ * item slot of a capacity fixed by the shape (B x Hkv + 16 waves of resident
+ * CTAs), then the combine: three launches, no host synchronisation, graph
+ * capturable.  If the rule's chunk would make more (request, kv head, chunk)
+ * items than the capacity, the chunk grows until they fit.  Workspace layout
+ * (offsets rounded up to 256 bytes): int32 plan[4] = {chunk_len, items,
+ * chunks of the longest request, capacity}; int32 pre[B + 1], the exclusive
+ * prefix over requests of their chunk counts; int4 items[capacity] = (b, kv
+ * head, chunk, clamped length) in (request, kv head, chunk) order; fp32
+ * partial outputs [capacity, rows, D] and partial LSEs [capacity, rows], item
+ * i = pre[b] * Hkv + kvh * n_b + s holding row r = t * G + g of that (b, kvh)
+ * (n_b = max(1, ceil(L_b / chunk_len)) chunks).  One request keeps the host
+ * plan (from max_seq_len) and, where it fits, the cluster merge.
  */
 int decode_attn(const decode_attn_params *p, const void *q, const void *k_cache,
                 const void *v_cache, const int32_t *block_table,
@@ -257,7 +279,9 @@ int decode_attn_split(const decode_attn_params *p, const void *q, const void *k_
  */
 /*   num_splits / chunk_len: the values the split pass used (num_splits ==
  *   ceil(max_seq_len / chunk_len)).  Launches nothing when that split pass
- *   merged through clusters (same params, same num_splits). */
+ *   merged through clusters (same params, same num_splits).  num_splits <= 0:
+ *   the split pass was device-planned; the chunk length, prefixes and
+ *   item-indexed partials are read from `workspace` (chunk_len is ignored). */
 int decode_attn_combine(const decode_attn_params *p, const int32_t *seq_lens,
                         int32_t num_splits, int32_t chunk_len,
                         const void *workspace, size_t workspace_bytes, void *out,
@@ -332,11 +356,26 @@ int decode_attn_host(const decode_attn_params *p, const void *q_host, const void
                      int32_t num_splits, void *workspace, size_t workspace_bytes,
                      int32_t *status_host, void *stream);
 
+/*
+ * The device planner alone: writes the plan, prefixes and item list that a
+ * device-planned decode_attn() call with these params would compute from
+ * seq_lens (layout under "Device planning" above) into `workspace`, without
+ * running the kernels that follow, so the plan can be read back and checked.
+ * The params must be ones decode_attn() plans on the device (two or more
+ * requests; tcgen05 shapes up to 1024 requests), else DA_ERR_BAD_SHAPE.
+ * DA_STATUS_SEQ_LEN / DA_STATUS_SHORT_CAUSAL are OR-ed into *status as the
+ * full call would.  Asynchronous; graph capturable.
+ */
+int decode_attn_device_plan(const decode_attn_params *p, const int32_t *seq_lens,
+                            void *workspace, size_t workspace_bytes, int32_t *status,
+                            void *stream);
+
 /* Static description of a return code. */
 const char *decode_attn_status_string(int code);
 
 /* Number of kernel launches decode_attn() makes for these arguments (1 or 2;
- * 1 with the cluster merge). */
+ * 1 with the cluster merge; 3 for a device-planned call: planner, split,
+ * combine). */
 int decode_attn_launch_count(const decode_attn_params *p, int32_t num_splits);
 
 #ifdef __cplusplus

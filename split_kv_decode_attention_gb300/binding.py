@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "decode_attn_params_init", "decode_attn_plan", "decode_attn_plan_slots", "decode_attn_chunk_len",
     "decode_attn_workspace_bytes", "decode_attn", "decode_attn_split", "decode_attn_combine",
     "decode_attn_status_string", "decode_attn_launch_count", "decode_attn_static_workspace",
-    "decode_attn_host_workspace_bytes", "decode_attn_host",
+    "decode_attn_host_workspace_bytes", "decode_attn_host", "decode_attn_device_plan",
 )
 DA_ERR_STATIC_WORKSPACE_LIMIT = -11
 STATIC_WORKSPACE_BYTES = 16 << 20
@@ -94,11 +94,13 @@ def lib() -> ctypes.CDLL:
         L.decode_attn_launch_count.argtypes = [P, i32]
         L.decode_attn_host_workspace_bytes.argtypes = [P, i32, ctypes.POINTER(sz)]
         L.decode_attn_host.argtypes = L.decode_attn.argtypes
+        L.decode_attn_device_plan.argtypes = [P, vp, vp, sz, vp, vp]
         for f in ("decode_attn_plan", "decode_attn_plan_slots", "decode_attn_chunk_len",
                   "decode_attn_workspace_bytes",
                   "decode_attn", "decode_attn_split", "decode_attn_combine",
                   "decode_attn_launch_count", "decode_attn_static_workspace",
-                  "decode_attn_host_workspace_bytes", "decode_attn_host"):
+                  "decode_attn_host_workspace_bytes", "decode_attn_host",
+                  "decode_attn_device_plan"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -222,7 +224,8 @@ def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
                 k_scale: float = 1.0, v_scale: float = 1.0):
     """Run decode attention; returns (out bf16 [B, q_len, Hq, D], lse fp32
     [B, q_len, Hq]).  Output, LSE and workspace tensors are allocated with
-    torch when not given; `num_splits <= 0` lets the library's planner choose."""
+    torch when not given; `num_splits <= 0` lets the library's planner choose
+    (on the device, from the lengths in `seq_lens`, for two or more requests)."""
     import torch
 
     B, T, Hq, D = q.shape
@@ -233,8 +236,7 @@ def decode_attn(q, k_cache, v_cache, block_table, seq_lens, *, max_seq_len: int,
     p = params if params is not None else params_from_tensors(
         q, k_cache, block_table, max_seq_len=max_seq_len, causal=causal, scale=scale, out=out,
         two_pass=two_pass, k_scale=k_scale, v_scale=v_scale)
-    if num_splits <= 0:
-        num_splits, _ = decode_attn_plan(p)
+    num_splits = max(0, int(num_splits))
     need = decode_attn_workspace_bytes(p, num_splits)
     if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty((need + 15) // 16 * 4, dtype=torch.float32, device=q.device)
@@ -289,10 +291,41 @@ def decode_attn_host(q_host, k_cache, v_cache, block_table_host, seq_lens_host, 
     return out_host, lse_host, status.value
 
 
+def decode_attn_device_plan(p: DecodeAttnParams, seq_lens, workspace, status=None, stream=None):
+    """Run the device planner alone (the first launch of a device-planned
+    decode_attn call) into `workspace`; read the plan back with
+    device_plan_view()."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().decode_attn_device_plan(ctypes.byref(p), _ptr(seq_lens), _ptr(workspace),
+                                         ws_bytes, _ptr(status), _stream_handle(stream)),
+           "decode_attn_device_plan")
+
+
+def device_plan_view(workspace, p: DecodeAttnParams):
+    """(plan int32[4] = chunk_len, items, chunks of the longest request,
+    capacity; pre int32[B + 1]; items int32[capacity, 4] = (b, kv head, chunk,
+    length)) views of a device-planned call's workspace, per the layout in the
+    header."""
+    import torch
+    b = workspace.view(-1).view(torch.int32)
+
+    def r256(x):
+        return (x + 255) // 256 * 256
+
+    plan = b[:4]
+    off = 256
+    pre = b[off // 4: off // 4 + p.batch + 1]
+    off = r256(off + (p.batch + 1) * 4)
+    cap = int(plan[3].item())
+    items = b[off // 4: off // 4 + 4 * cap].view(cap, 4)
+    return plan, pre, items
+
+
 def decode_attn_combine(p: DecodeAttnParams, seq_lens, num_splits: int, chunk_len: int,
                         workspace, out, lse, stream=None):
     """Merge the partials held in `workspace` into out/lse (rows of requests
-    spanning two or more chunks)."""
+    spanning two or more chunks); num_splits <= 0 after a device-planned
+    split pass."""
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().decode_attn_combine(ctypes.byref(p), _ptr(seq_lens), int(num_splits),
                                      int(chunk_len), _ptr(workspace), ws_bytes, _ptr(out),

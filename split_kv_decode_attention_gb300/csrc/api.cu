@@ -13,6 +13,7 @@
 
 #include "decode_attn.h"
 #include "kernels.cuh"
+#include "plan_rule.cuh"
 
 namespace {
 
@@ -20,20 +21,6 @@ using dattn::kHeadDim;
 using dattn::kTileTokens;
 
 constexpr int kMaxDevices = 64;
-// Planner: a chunk is never shorter than this many tokens (partials and the
-// combine cost ~1.5 KB per row per chunk; a 16 KB+ chunk read keeps that small).
-constexpr int kMinChunkTokens = 256;
-// Ragged batches: chunks are sized for this many waves of resident CTAs over
-// the batch's total work, and hold at least kTokensPerRow tokens per query row
-// (fit on GB300 sweeps of chunk length: ~1-2K tokens for 4-16 rows).
-constexpr int kRaggedWaves = 8;
-constexpr int kTokensPerRow = 64;
-// The tcgen05 kernel (17..128 rows) pays ~3 us per work item (epilogue,
-// the two softmax groups' merge), so its chunks hold twice that (w64: 2
-// chunks of 8K instead of 4 of 4K, ~1.5 % faster).
-constexpr int kWideTokensPerRow = 128;
-// Largest thread-block cluster the split kernel uses (non-portable size).
-constexpr int kMaxClusterSplits = 16;
 
 struct DeviceInfo {
   int sm_count = 0;
@@ -115,72 +102,42 @@ int check_paged(const decode_attn_params* p, bool paged) {
 
 int chunk_for_splits(const decode_attn_params* p, int32_t num_splits, int32_t* chunk,
                      int32_t* splits_eff) {
-  if (num_splits < 1) return DA_ERR_SPLITS;
-  const int64_t L = p->max_seq_len;
-  int64_t c = ceil_div64(std::max<int64_t>(L, 1), num_splits);
-  c = ceil_div64(c, kTileTokens) * kTileTokens;
-  if (c > (1LL << 30)) return DA_ERR_SPLITS;
-  *chunk = static_cast<int32_t>(c);
-  *splits_eff = static_cast<int32_t>(std::max<int64_t>(1, ceil_div64(L, c)));
-  return DA_OK;
+  return dattn::plan_chunk_for_splits(p->max_seq_len, num_splits, chunk, splits_eff)
+             ? DA_OK
+             : DA_ERR_SPLITS;
 }
 
-// The planner proper: a function of the shape, the host lengths and the
-// number of CTAs the split launch keeps resident at once (SMs x CTAs per SM).
+// The planner proper (the rule of plan_rule.cuh, shared with the device
+// planner kernel): a function of the shape, the host lengths and the number
+// of CTAs the split launch keeps resident at once (SMs x CTAs per SM).
 int plan_for_slots(const decode_attn_params* p, const int32_t* host_seq_lens, int64_t slots,
                    int32_t* num_splits, int32_t* chunk_len) {
-  const int rows = rows_of(p);
-  const int64_t max_tiles = ceil_div64(std::max(p->max_seq_len, 1), kTileTokens);
-  const int64_t pairs = static_cast<int64_t>(std::max(p->batch, 1)) * p->num_kv_heads;
+  dattn::PlanShape shape;
+  shape.slots = slots;
+  shape.batch = p->batch;
+  shape.num_kv_heads = p->num_kv_heads;
+  shape.rows = rows_of(p);
+  shape.max_seq_len = p->max_seq_len;
   bool uniform = true;
   int64_t work_tokens = 0;
+  auto clamped = [&](int32_t b) {
+    return std::min<int64_t>(std::max(host_seq_lens[b], 0), p->max_seq_len);
+  };
   if (host_seq_lens != nullptr) {
     for (int32_t b = 0; b < p->batch; ++b) {
-      const int64_t Lb = std::min<int64_t>(std::max(host_seq_lens[b], 0), p->max_seq_len);
-      work_tokens += Lb;
+      work_tokens += clamped(b);
       if (host_seq_lens[b] != host_seq_lens[0]) uniform = false;
     }
   }
-  int64_t splits = 1;
-  int64_t min_chunk = kMinChunkTokens;
-  if (uniform) {
-    // equal lengths: one full wave of equal chunks -- as many chunks per
-    // (request, kv head) as there are resident CTA slots for them, at most
-    // kMaxClusterSplits so that the chunks of a head can merge as a cluster
-    if (pairs < slots) splits = std::min<int64_t>(slots / pairs, kMaxClusterSplits);
-  } else {
-    // ragged lengths: ~kRaggedWaves waves of chunks over the actual work, so
-    // long requests are cut into pieces that keep the tail short; a chunk
-    // costs rows x 516 B of partials written and read back, so chunks grow
-    // with the row count (kTokensPerRow tokens per query row at least)
-    const int64_t per_cta = ceil_div64(work_tokens * p->num_kv_heads, kRaggedWaves * slots);
-    const int per_row = rows > dattn::kMaxNarrowRows ? kWideTokensPerRow : kTokensPerRow;
-    min_chunk = std::max<int64_t>(kMinChunkTokens, static_cast<int64_t>(per_row) * rows);
-    int64_t target = std::max<int64_t>(min_chunk, per_cta);
-    // ... but a small batch keeps at least one chunk per CTA slot: while the
-    // per-row floor leaves fewer chunks than slots, the chunk shrinks (to the
-    // largest length that fills them, not below kMinChunkTokens)
-    auto chunks_of = [&](int64_t c) {
-      int64_t n = 0;
-      for (int32_t b = 0; b < p->batch; ++b) {
-        const int64_t Lb = std::min<int64_t>(std::max(host_seq_lens[b], 0), p->max_seq_len);
-        n += Lb > 0 ? ceil_div64(Lb, c) : 1;
-      }
-      return n * p->num_kv_heads;
-    };
-    if (target > kMinChunkTokens && chunks_of(target) < slots) {
-      int64_t lo = kMinChunkTokens, hi = target;  // chunks_of(hi) < slots
-      while (hi - lo > 1) {
-        const int64_t mid = (lo + hi) / 2;
-        if (chunks_of(mid) >= slots) lo = mid;
-        else hi = mid;
-      }
-      target = lo;
+  auto chunks_of = [&](int64_t c) {
+    int64_t n = 0;
+    for (int32_t b = 0; b < p->batch; ++b) {
+      const int64_t Lb = clamped(b);
+      n += Lb > 0 ? ceil_div64(Lb, c) : 1;
     }
-    splits = ceil_div64(std::max(p->max_seq_len, 1), target);
-  }
-  splits = std::min<int64_t>(splits, std::max<int64_t>(1, p->max_seq_len / kMinChunkTokens));
-  splits = std::max<int64_t>(1, std::min<int64_t>(splits, max_tiles));
+    return n * p->num_kv_heads;
+  };
+  const int64_t splits = dattn::plan_splits(shape, uniform, work_tokens, chunks_of);
   int32_t chunk = 0, eff = 0;
   const int rc = chunk_for_splits(p, static_cast<int32_t>(splits), &chunk, &eff);
   if (rc != DA_OK) return rc;
@@ -242,6 +199,89 @@ bool use_cluster_merge(const decode_attn_params* p, int32_t splits_eff) {
   if ((p->flags & DA_FLAG_TWO_PASS) != 0 || splits_eff < 2 || p->batch < 1) return false;
   return dattn::split_cluster_merge_fits(rows_of(p), kv_fp8(p), splits_eff,
                                          static_cast<int64_t>(p->batch) * p->num_kv_heads);
+}
+
+// ---- device-planned calls
+// decode_attn(num_splits <= 0) with two or more requests plans on the device:
+// the lengths may exist only in device memory (and change between replays of
+// a captured graph), so a planner kernel applies the planner's rule to them
+// and writes a work list; the split launch has one CTA per item slot of a
+// host-sized capacity and the partials are indexed by item, so nothing the
+// host sizes depends on the lengths.  A single request keeps the host plan
+// (its only length is bounded by max_seq_len), with the cluster merge.
+// Capacity: at most B * Hkv items of one chunk each, plus about 2 x
+// kRaggedWaves waves of resident CTAs (the rule aims at kRaggedWaves; its
+// rounding can double that); the planner grows the chunk if a plan would
+// exceed it.
+constexpr int64_t kListWaveSlack = 2 * dattn::kRaggedWaves;
+
+struct ListLayout {
+  size_t plan, pre, items, part_o, part_lse, total;
+  int64_t cap, slots;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool device_planned(const decode_attn_params* p, int32_t num_splits) {
+  // (the tcgen05 kernel walks its items persistently, from tables of at most
+  // kWideMaxPlannedBatch requests)
+  return num_splits <= 0 && p->batch >= 2 && p->max_seq_len <= (1 << 30) &&
+         (rows_of(p) <= dattn::kMaxNarrowRows || p->batch <= dattn::kWideMaxPlannedBatch);
+}
+
+// Resident CTAs of the split launch for this shape on the current device.
+int split_slots(const decode_attn_params* p, int64_t* slots) {
+  DeviceInfo di;
+  const int rc = current_device_info(&di);
+  if (rc != DA_OK) return rc;
+  *slots = static_cast<int64_t>(di.sm_count) * dattn::split_ctas_per_sm(rows_of(p), kv_fp8(p));
+  return DA_OK;
+}
+
+// Workspace of a device-planned call (offsets 256-byte aligned): plan[4],
+// pre[B + 1], items[cap] (int4), partial outputs [cap, rows, D] and partial
+// LSEs [cap, rows] (fp32).
+int list_layout(const decode_attn_params* p, ListLayout* l) {
+  int rc = split_slots(p, &l->slots);
+  if (rc != DA_OK) return rc;
+  l->cap = static_cast<int64_t>(p->batch) * p->num_kv_heads + kListWaveSlack * l->slots;
+  if (l->cap > 0x7fffffff) return DA_ERR_BAD_SHAPE;
+  const size_t rows = static_cast<size_t>(rows_of(p));
+  const size_t cap = static_cast<size_t>(l->cap);
+  size_t off = 0;
+  l->plan = off;
+  off = round256(off + 16);
+  l->pre = off;
+  off = round256(off + (static_cast<size_t>(p->batch) + 1) * 4);
+  l->items = off;
+  off = round256(off + cap * 16);
+  l->part_o = off;
+  off = round256(off + cap * rows * kHeadDim * 4);
+  l->part_lse = off;
+  l->total = off + cap * rows * 4;
+  return DA_OK;
+}
+
+// Arguments of the planner kernel for a device-planned call whose workspace
+// starts at w.
+dattn::PlanArgs plan_args(const decode_attn_params* p, const int32_t* seq_lens, int32_t* status,
+                          uint8_t* w, const ListLayout& lay) {
+  dattn::PlanArgs pa;
+  std::memset(&pa, 0, sizeof(pa));
+  pa.seq_lens = seq_lens;
+  pa.status = status;
+  pa.plan = reinterpret_cast<int32_t*>(w + lay.plan);
+  pa.pre = reinterpret_cast<int32_t*>(w + lay.pre);
+  pa.items = reinterpret_cast<int4*>(w + lay.items);
+  pa.slots = lay.slots;
+  pa.cap = lay.cap;
+  pa.batch = p->batch;
+  pa.num_kv_heads = p->num_kv_heads;
+  pa.rows = rows_of(p);
+  pa.max_seq_len = p->max_seq_len;
+  pa.q_len = p->q_len;
+  pa.causal = p->causal ? 1 : 0;
+  return pa;
 }
 
 }  // namespace
@@ -308,7 +348,18 @@ int decode_attn_workspace_bytes(const decode_attn_params* p, int32_t num_splits,
   int rc = check_shape(p);
   if (rc != DA_OK) return rc;
   if (bytes == nullptr) return DA_ERR_NULL_POINTER;
+  if (device_planned(p, num_splits)) {
+    ListLayout l;
+    rc = list_layout(p, &l);
+    if (rc != DA_OK) return rc;
+    *bytes = l.total;
+    return DA_OK;
+  }
   int32_t chunk = 0, eff = 0;
+  if (num_splits <= 0) {  // one request (or none): the host plan
+    rc = plan_impl(p, nullptr, &num_splits, &chunk);
+    if (rc != DA_OK) return rc;
+  }
   rc = chunk_for_splits(p, num_splits, &chunk, &eff);
   if (rc != DA_OK) return rc;
   if (eff <= 1) {
@@ -324,6 +375,7 @@ int decode_attn_launch_count(const decode_attn_params* p, int32_t num_splits) {
   int rc = check_shape(p);
   if (rc != DA_OK) return rc;
   if (p->batch == 0) return 0;
+  if (device_planned(p, num_splits)) return 3;  // planner, split, combine
   int32_t chunk = 0, eff = 0;
   if (num_splits <= 0) {
     rc = plan_impl(p, nullptr, &num_splits, &chunk);
@@ -371,19 +423,29 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   if (rc != DA_OK) return rc;
   if (di.major * 10 + di.minor < 100) return DA_ERR_NO_DEVICE;
 
+  const bool listed = device_planned(p, num_splits);
+  ListLayout lay;
   int32_t chunk = 0, eff = 0;
-  if (num_splits <= 0) {
-    rc = plan_impl(p, nullptr, &num_splits, &chunk);
+  bool cluster_merge = false;
+  if (listed) {
+    rc = list_layout(p, &lay);
     if (rc != DA_OK) return rc;
+    if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
+      return DA_ERR_WORKSPACE;
+  } else {
+    if (num_splits <= 0) {
+      rc = plan_impl(p, nullptr, &num_splits, &chunk);
+      if (rc != DA_OK) return rc;
+    }
+    rc = chunk_for_splits(p, num_splits, &chunk, &eff);
+    if (rc != DA_OK) return rc;
+    cluster_merge = use_cluster_merge(p, eff);
+    size_t need = 0;
+    decode_attn_workspace_bytes(p, num_splits, &need);
+    if (!cluster_merge && need > 0 &&
+        (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+      return DA_ERR_WORKSPACE;
   }
-  rc = chunk_for_splits(p, num_splits, &chunk, &eff);
-  if (rc != DA_OK) return rc;
-  const bool cluster_merge = use_cluster_merge(p, eff);
-  size_t need = 0;
-  decode_attn_workspace_bytes(p, num_splits, &need);
-  if (!cluster_merge && need > 0 &&
-      (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
-    return DA_ERR_WORKSPACE;
 
   CUtensorMap kmap, vmap;
   std::memset(&kmap, 0, sizeof(kmap));
@@ -432,9 +494,27 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   a.v_scale = kv_fp8(p) ? p->v_scale : 1.f;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if (listed) {
+    // the planner writes the plan, prefixes and items; the split launch has
+    // one CTA per item slot and stores partials by item
+    a.plan = reinterpret_cast<const int32_t*>(w + lay.plan);
+    a.pre = reinterpret_cast<const int32_t*>(w + lay.pre);
+    a.items = reinterpret_cast<const int4*>(w + lay.items);
+    a.item_slots = static_cast<int>(lay.cap);
+    a.part_o = reinterpret_cast<float*>(w + lay.part_o);
+    a.part_lse = reinterpret_cast<float*>(w + lay.part_lse);
+    a.chunk_len = 0;
+    a.num_splits = 1;
+    if (dattn::launch_plan(plan_args(p, seq_lens, status, w, lay), st) != cudaSuccess)
+      return DA_ERR_CUDA;
+  }
   if (dattn::launch_split(kmap, vmap, a, cluster_merge, st) != cudaSuccess) return DA_ERR_CUDA;
-  if (run_combine && eff > 1 && !cluster_merge) {
-    dattn::CombineArgs c;
+  if (run_combine && (listed || (eff > 1 && !cluster_merge))) {
+    dattn::CombineArgs c = {};
+    c.plan = a.plan;
+    c.pre = a.pre;
+    c.num_kv_heads = p->num_kv_heads;
     c.part_o = a.part_o;
     c.part_lse = a.part_lse;
     c.seq_lens = seq_lens;
@@ -481,21 +561,39 @@ int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens, in
   if (rc != DA_OK) return rc;
   if (p->batch == 0) return DA_OK;
   if (seq_lens == nullptr || out == nullptr || lse == nullptr) return DA_ERR_NULL_POINTER;
-  if (num_splits < 1 || chunk_len < 1 || chunk_len % kTileTokens != 0 ||
-      ceil_div64(std::max(p->max_seq_len, 1), chunk_len) != num_splits)
+  const bool listed = device_planned(p, num_splits);
+  if (!listed && (num_splits < 1 || chunk_len < 1 || chunk_len % kTileTokens != 0 ||
+                  ceil_div64(std::max(p->max_seq_len, 1), chunk_len) != num_splits))
     return DA_ERR_SPLITS;
-  if (use_cluster_merge(p, num_splits)) return DA_OK;  // the split pass already merged
+  if (!listed && use_cluster_merge(p, num_splits)) return DA_OK;  // the split pass merged
   if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
       !stride_ok(p->o_stride_batch) || !stride_ok(p->o_stride_token) ||
       !stride_ok(p->o_stride_head))
     return DA_ERR_ALIGNMENT;
   const size_t rows_total = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
-  const size_t need = rows_total * static_cast<size_t>(num_splits) * (kHeadDim + 1) * sizeof(float);
-  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
-    return DA_ERR_WORKSPACE;
-  dattn::CombineArgs c;
-  c.part_o = static_cast<const float*>(workspace);
-  c.part_lse = c.part_o + rows_total * num_splits * kHeadDim;
+  dattn::CombineArgs c = {};
+  if (listed) {
+    // the plan, prefixes and item-indexed partials a device-planned split
+    // pass left in the workspace (num_splits <= 0 there too)
+    ListLayout lay;
+    rc = list_layout(p, &lay);
+    if (rc != DA_OK) return rc;
+    if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
+      return DA_ERR_WORKSPACE;
+    const uint8_t* w = static_cast<const uint8_t*>(workspace);
+    c.plan = reinterpret_cast<const int32_t*>(w + lay.plan);
+    c.pre = reinterpret_cast<const int32_t*>(w + lay.pre);
+    c.part_o = reinterpret_cast<const float*>(w + lay.part_o);
+    c.part_lse = reinterpret_cast<const float*>(w + lay.part_lse);
+    c.num_kv_heads = p->num_kv_heads;
+  } else {
+    const size_t need =
+        rows_total * static_cast<size_t>(num_splits) * (kHeadDim + 1) * sizeof(float);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+      return DA_ERR_WORKSPACE;
+    c.part_o = static_cast<const float*>(workspace);
+    c.part_lse = c.part_o + rows_total * num_splits * kHeadDim;
+  }
   c.seq_lens = seq_lens;
   c.out = static_cast<uint16_t*>(out);
   c.o_sb = p->o_stride_batch;
@@ -524,7 +622,6 @@ struct HostLayout {
   size_t part, q, out, lse, lens, bt, status, total;
 };
 
-size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int host_layout(const decode_attn_params* p, int32_t num_splits, bool paged, HostLayout* h) {
   size_t part = 0;
@@ -652,6 +749,29 @@ int decode_attn_host(const decode_attn_params* p, const void* q_host, const void
        cudaMemcpyAsync(status_host, w + h.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess))
     return finish(DA_ERR_CUDA);
   return finish(DA_OK);
+}
+
+int decode_attn_device_plan(const decode_attn_params* p, const int32_t* seq_lens,
+                            void* workspace, size_t workspace_bytes, int32_t* status,
+                            void* stream) {
+  int rc = check_shape(p);
+  if (rc != DA_OK) return rc;
+  if (!device_planned(p, 0)) return DA_ERR_BAD_SHAPE;
+  if (seq_lens == nullptr) return DA_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0) return DA_ERR_ALIGNMENT;
+  DeviceInfo di;
+  rc = current_device_info(&di);
+  if (rc != DA_OK) return rc;
+  if (di.major * 10 + di.minor < 100) return DA_ERR_NO_DEVICE;
+  ListLayout lay;
+  rc = list_layout(p, &lay);
+  if (rc != DA_OK) return rc;
+  if (workspace == nullptr || workspace_bytes < lay.total || !aligned16(workspace))
+    return DA_ERR_WORKSPACE;
+  if (dattn::launch_plan(plan_args(p, seq_lens, status, static_cast<uint8_t*>(workspace), lay),
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return DA_OK;
 }
 
 const char* decode_attn_status_string(int code) {

@@ -22,7 +22,12 @@ constexpr int kWarpsPerBlock = 8;
 constexpr int kBlocksPerSm = 6;  // registers capped so that 48 warps fit per SM
 constexpr float kLog2e = 1.4426950408889634f;
 
-__global__ void __launch_bounds__(32 * kWarpsPerBlock, kBlocksPerSm)
+// LISTED: a device-planned call (partials indexed by item, chunk length from
+// the planner's output); otherwise partials are [row][split].
+// (the device-planned form holds more addressing state: 5 blocks per SM, no
+// spills, instead of 6)
+template <bool LISTED>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock, LISTED ? kBlocksPerSm - 1 : kBlocksPerSm)
     combine_kernel(const CombineArgs a) {
   constexpr uint32_t kFull = 0xffffffffu;
   const int warp = threadIdx.x >> 5;
@@ -33,35 +38,68 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock, kBlocksPerSm)
   const int h = live ? static_cast<int>(row % a.num_q_heads) : 0;
   const int t = live ? static_cast<int>((row / a.num_q_heads) % a.q_len) : 0;
   const int b = live ? static_cast<int>(row / (static_cast<int64_t>(a.num_q_heads) * a.q_len)) : 0;
-  const int S = a.num_splits;
-  const float* pl = a.part_lse + row * S;
-  const float* po = a.part_o + row * S * kHeadDim + lane * 4;
   // the split kernel that wrote the partials may still be running (this
   // kernel may launch during its tail): wait before reading anything
   grid_dependency_wait();
   if (!live) return;
 
-  // one round trip for the request length, the first 32 LSEs and the first
-  // kBatch partial rows: none of these loads depends on another. Splits past
-  // the request's chunk count hold stale values, dropped by the selects below.
+  // Partial s of this row is at pl[s * ls] / po[s * os].  Grid-planned call:
+  // [row][split] (ls = 1, os = D).  Device-planned call: by item, item(b,
+  // kvh, s) = pre[b] * Hkv + kvh * n + s, row r of the item's rows (ls =
+  // rows, os = rows * D); its base needs the request's prefix and the
+  // chunk length first (one more round trip).
   constexpr int kBatch = 4;
   const uint64_t dead = l2_evict_first_policy();  // each partial is read once
-  int L = a.seq_lens[b];
-  const float lse0 = lane < S ? ld_global_hint1(pl + lane, dead) : -INFINITY;
+  const float* pl;
+  const float* po;
+  int ls, os;  // per-split strides (<= 128 rows x 128 d)
+  int S, L, n;
+  if constexpr (LISTED) {
+    L = a.seq_lens[b];
+    const int pb = a.pre[b];
+    const int chunk = a.plan[0];
+    L = L < 0 ? 0 : (L > a.max_seq_len ? a.max_seq_len : L);
+    n = L > 0 ? (L + chunk - 1) / chunk : 1;
+    if (n < 2) return;  // the split kernel wrote this row directly
+    const int G = a.num_q_heads / a.num_kv_heads;
+    const int rows = G * a.q_len;
+    const int kvh = h / G;
+    const int64_t base = static_cast<int64_t>(pb) * a.num_kv_heads + static_cast<int64_t>(kvh) * n;
+    const int64_t r0 = base * rows + t * G + (h - kvh * G);
+    pl = a.part_lse + r0;
+    po = a.part_o + r0 * kHeadDim + lane * 4;
+    ls = rows;
+    os = rows * kHeadDim;
+    S = n;
+  } else {
+    S = a.num_splits;
+    pl = a.part_lse + row * S;
+    po = a.part_o + row * S * kHeadDim + lane * 4;
+    ls = 1;
+    os = kHeadDim;
+    L = a.seq_lens[b];
+    n = 0;  // known after the first round trip
+  }
+  // one round trip for the first 32 LSEs and the first kBatch partial rows
+  // (grid-planned: with the request length): none of these loads depends on
+  // another. Splits past the request's chunk count hold stale values,
+  // dropped by the selects below.
+  const float lse0 = lane < S ? ld_global_hint1(pl + lane * ls, dead) : -INFINITY;
   float4 v[kBatch];
 #pragma unroll
   for (int j = 0; j < kBatch; ++j)
-    v[j] = j < S ? ld_global_hint(po + static_cast<int64_t>(j) * kHeadDim, dead)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-  L = L < 0 ? 0 : (L > a.max_seq_len ? a.max_seq_len : L);
-  const int n = L > 0 ? (L + a.chunk_len - 1) / a.chunk_len : 1;
-  if (n < 2) return;  // the split kernel wrote this row directly
+    v[j] = j < S ? ld_global_hint(po + j * os, dead) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (!LISTED) {
+    L = L < 0 ? 0 : (L > a.max_seq_len ? a.max_seq_len : L);
+    n = L > 0 ? (L + a.chunk_len - 1) / a.chunk_len : 1;
+    if (n < 2) return;  // the split kernel wrote this row directly
+  }
 
   uint16_t* orow = a.out + static_cast<int64_t>(b) * a.o_sb + static_cast<int64_t>(t) * a.o_st +
                    static_cast<int64_t>(h) * a.o_sh + lane * 4;
   // splits in groups of 32: lane j holds lse of split s0 + j
   float M = lane < n ? lse0 : -INFINITY;
-  for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, ld_global_hint1(pl + s, dead));
+  for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, ld_global_hint1(pl + s * ls, dead));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 16));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 8));
   M = fmaxf(M, __shfl_xor_sync(kFull, M, 4));
@@ -76,13 +114,14 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock, kBlocksPerSm)
   float W = 0.f;
   for (int s0 = 0; s0 < n; s0 += 32) {
     const int cnt = min(32, n - s0);
-    const float lse_mine = s0 == 0 ? lse0 : (lane < cnt ? ld_global_hint1(pl + s0 + lane, dead) : -INFINITY);
+    const float lse_mine =
+        s0 == 0 ? lse0 : (lane < cnt ? ld_global_hint1(pl + (s0 + lane) * ls, dead) : -INFINITY);
     const float w_mine = lane < cnt ? ex2((lse_mine - M) * kLog2e) : 0.f;
     for (int j0 = 0; j0 < cnt; j0 += kBatch) {
       if (s0 + j0 > 0) {  // batch 0 of group 0 is already in flight
 #pragma unroll
         for (int j = 0; j < kBatch; ++j)
-          v[j] = j0 + j < cnt ? ld_global_hint(po + static_cast<int64_t>(s0 + j0 + j) * kHeadDim, dead)
+          v[j] = j0 + j < cnt ? ld_global_hint(po + (s0 + j0 + j) * os, dead)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
@@ -119,7 +158,8 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+  return a.plan != nullptr ? cudaLaunchKernelEx(&cfg, combine_kernel<true>, a)
+                           : cudaLaunchKernelEx(&cfg, combine_kernel<false>, a);
 }
 
 }  // namespace dattn

@@ -14,6 +14,7 @@ constexpr int kHeadDim = 128;
 constexpr int kTileTokens = 16;        // tokens per TMA box / per MMA tile
 constexpr int kMaxRows = 128;          // GQA group x q_len rows per CTA
 constexpr int kMaxNarrowRows = 16;     // above this: the tcgen05 kernel
+constexpr int kWideMaxPlannedBatch = 1024;  // tcgen05 kernel: device-planned calls up to this batch
 
 // Arguments of the split kernel (one CTA per (chunk, kv head, request)).
 struct SplitArgs {
@@ -37,6 +38,28 @@ struct SplitArgs {
   int kv_fp8;                          // caches hold FP8 E4M3
   float v_scale;                       // FP8: values = v_scale * V (k_scale is in scale_log2)
   int test_withhold;                   // DA_FLAG_TEST_WITHHOLD_COPY (narrow kernel, two-pass)
+  // Device-planned calls (items != nullptr): the planner kernel wrote the
+  // chunk length and item count to plan[0..1], per-request prefixes of chunk
+  // counts to pre[], and the work items (b, kv head, chunk, clamped length) to
+  // items[]; the split grid is `item_slots` CTAs (one per possible item) and
+  // partial (item i, row r) sits at part_o[(i * rows + r) * D] / part_lse[i *
+  // rows + r].  chunk_len / num_splits above are unused then.
+  const int4* items;
+  const int32_t* plan;
+  const int32_t* pre;
+  int item_slots;
+};
+
+// Arguments of the device planner kernel (one CTA; plan_kernel.cu).
+struct PlanArgs {
+  const int32_t* seq_lens;
+  int32_t* status;                     // optional
+  int32_t* plan;                       // [4]: chunk_len, n_items, max chunks, capacity
+  int32_t* pre;                        // [B + 1]
+  int4* items;                         // [cap]
+  int64_t slots;                       // resident CTAs of the split launch
+  int64_t cap;                         // item slots of the split launch
+  int batch, num_kv_heads, rows, max_seq_len, q_len, causal;
 };
 
 struct CombineArgs {
@@ -48,6 +71,11 @@ struct CombineArgs {
   float* lse;
   int batch, q_len, num_q_heads;
   int max_seq_len, chunk_len, num_splits;
+  // device-planned calls (plan != nullptr): chunk length from plan[0],
+  // partials indexed by item (see SplitArgs)
+  const int32_t* plan;
+  const int32_t* pre;
+  int num_kv_heads;
 };
 
 // Physical page ids of a chunk's 16-token tiles, for the TMA producer warp.
@@ -107,5 +135,8 @@ int wide_ctas_per_sm();
 
 // Launch the combine kernel (one warp per output row).
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+// Launch the device planner (one CTA) ahead of a device-planned split launch.
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 
 }  // namespace dattn

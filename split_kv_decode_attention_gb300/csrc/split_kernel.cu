@@ -107,27 +107,42 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
                     const __grid_constant__ CUtensorMap v_map, const SplitArgs a) {
   using C = SplitCfg<NT, STAGES, TPS, F8>;
   constexpr uint32_t kFull = 0xffffffffu;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const bool listed = !CM && a.items != nullptr;  // device-planned call
 
-  // launched early behind the previous kernel of the stream: nothing that
-  // kernel may write (q, caches, lengths, outputs) is touched before this
+  // launched early behind the previous kernel of the stream (or the device
+  // planner): nothing it may write (q, caches, lengths, the plan, outputs)
+  // is touched before this
   grid_dependency_wait();
 
-  // ---- this CTA's key range [t_begin, t_end)
-  int L = a.seq_lens[b];
-  uint32_t bad = 0;
-  if (L < 0 || L > a.max_seq_len) {
-    bad |= DA_STATUS_SEQ_LEN;
-    L = L < 0 ? 0 : a.max_seq_len;
+  // ---- this CTA's work item and key range [t_begin, t_end)
+  int split, kvh, b, L, chunk;
+  if (listed) {
+    // item slot blockIdx.x of the planner's list (slots past its count exit)
+    const int n_items = a.plan[1];
+    const int4 itm = a.items[blockIdx.x];
+    chunk = a.plan[0];
+    if (static_cast<int>(blockIdx.x) >= n_items) return;
+    b = itm.x;
+    kvh = itm.y;
+    split = itm.z;
+    L = itm.w;  // clamped (and reported) by the planner
+  } else {
+    split = blockIdx.x;
+    kvh = blockIdx.y;
+    b = blockIdx.z;
+    L = a.seq_lens[b];
+    uint32_t bad = 0;
+    if (L < 0 || L > a.max_seq_len) {
+      bad |= DA_STATUS_SEQ_LEN;
+      L = L < 0 ? 0 : a.max_seq_len;
+    }
+    if (a.causal && L > 0 && L < a.q_len) bad |= DA_STATUS_SHORT_CAUSAL;
+    if (bad && a.status != nullptr && split == 0 && kvh == 0 && threadIdx.x == 0)
+      atomicOr(a.status, static_cast<int32_t>(bad));
+    chunk = a.chunk_len;
   }
-  if (a.causal && L > 0 && L < a.q_len) bad |= DA_STATUS_SHORT_CAUSAL;
-  if (bad && a.status != nullptr && split == 0 && kvh == 0 && threadIdx.x == 0)
-    atomicOr(a.status, static_cast<int32_t>(bad));
-  const int chunk = a.chunk_len;
   const int nsplit_b = L > 0 ? (L + chunk - 1) / chunk : 1;
   // (with the cluster merge every CTA stays: an empty chunk contributes 0 / -inf)
   if (!CM && split >= nsplit_b) return;
@@ -595,27 +610,51 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     }
     cluster_sync();  // every CTA's (O, lse) is visible cluster-wide
 
-    const int S = gridDim.x;  // cluster = all chunks of this (kv head, request)
+    const int S = gridDim.x;  // cluster = all chunks of this (kv head, request), <= 16
     const uint32_t xo_addr = smem_addr(xo);
     const uint32_t xl_addr = smem_addr(xl);
     for (int u = split * 32 * TPS + threadIdx.x; u < a.rows * 32; u += S * 32 * TPS) {
       const int row = u >> 5;
       const int d = (u & 31) * 4;
+      // every peer's LSE and the first 8 peers' output slices in one round
+      // trip of independent remote loads, the other 8 in a second (a load
+      // consumed right after it is issued would cost a round trip per peer)
+      constexpr int kPeers = 16, kHalf = 8;
+      float lr[kPeers];
+      float4 x[kHalf];
+#pragma unroll
+      for (int r = 0; r < kPeers; ++r)
+        lr[r] = r < S ? ld_cluster_f32(map_to_rank(xl_addr + row * 4, r)) : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kHalf; ++j)
+        x[j] = j < S ? ld_cluster_f32x4(map_to_rank(xo_addr + (row * kHeadDim + d) * 4, j))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
       float M = -INFINITY;
-      for (int r = 0; r < S; ++r)
-        M = fmaxf(M, ld_cluster_f32(map_to_rank(xl_addr + row * 4, r)));
+#pragma unroll
+      for (int r = 0; r < kPeers; ++r) M = fmaxf(M, lr[r]);
       float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
       float W = 0.f;
       if (M != -INFINITY) {
-        for (int r = 0; r < S; ++r) {
-          const float w = ex2((ld_cluster_f32(map_to_rank(xl_addr + row * 4, r)) - M) * kLog2e);
-          const float4 x =
-              ld_cluster_f32x4(map_to_rank(xo_addr + (row * kHeadDim + d) * 4, r));
-          W += w;
-          acc4.x += w * x.x;
-          acc4.y += w * x.y;
-          acc4.z += w * x.z;
-          acc4.w += w * x.w;
+#pragma unroll
+        for (int r0 = 0; r0 < kPeers; r0 += kHalf) {
+          if (r0 > 0 && r0 < S) {
+#pragma unroll
+            for (int j = 0; j < kHalf; ++j)
+              x[j] = r0 + j < S
+                         ? ld_cluster_f32x4(map_to_rank(xo_addr + (row * kHeadDim + d) * 4, r0 + j))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < kHalf; ++j) {
+            if (r0 + j < S) {  // peers in rank order: the sums of the earlier form
+              const float w = ex2((lr[r0 + j] - M) * kLog2e);
+              W += w;
+              acc4.x += w * x[j].x;
+              acc4.y += w * x[j].y;
+              acc4.z += w * x[j].z;
+              acc4.w += w * x[j].w;
+            }
+          }
         }
       }
       const float inv = W > 0.f ? 1.f / W : 0.f;
@@ -657,7 +696,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
                                   static_cast<int64_t>(h) * a.o_sh + d) = pk;
       } else {
         const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
-        st_global_hint(a.part_o + (prow * S + split) * kHeadDim + d, v, l2_evict_last_policy());
+        const int64_t pidx = listed ? static_cast<int64_t>(blockIdx.x) * a.rows + row
+                                    : prow * S + split;
+        st_global_hint(a.part_o + pidx * kHeadDim + d, v, l2_evict_last_policy());
       }
     }
     if (threadIdx.x < a.rows) {
@@ -677,7 +718,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
       if (direct)
         a.lse[prow] = lse;
       else
-        st_global_hint(a.part_lse + prow * S + split, lse, l2_evict_last_policy());
+        st_global_hint(a.part_lse + (listed ? static_cast<int64_t>(blockIdx.x) * a.rows + row
+                                            : prow * S + split),
+                       lse, l2_evict_last_policy());
     }
   }
 }
@@ -779,7 +822,8 @@ template <int NT, bool CM, bool F8, bool DP>
 void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const SplitArgs& a,
                  cudaStream_t st) {
   cfg = {};
-  cfg.gridDim = dim3(a.num_splits, a.num_kv_heads, a.batch);
+  cfg.gridDim = a.items != nullptr ? dim3(static_cast<unsigned>(a.item_slots))
+                                   : dim3(a.num_splits, a.num_kv_heads, a.batch);
   cfg.blockDim = dim3(Variant<NT, CM, F8, DP>::C::kThreads);
   cfg.dynamicSmemBytes = Variant<NT, CM, F8, DP>::C::kSmemBytes;
   cfg.stream = st;
@@ -807,9 +851,17 @@ cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitA
   return cudaLaunchKernelEx(&cfg, Variant<NT, CM, F8, DP>::kernel, km, vm, a);
 }
 
+// Resident CTAs per SM of a variant (queried once per device, then cached).
+int g_ctas_per_sm[2][2][kMaxDev];
+
 template <int NT, bool F8>
 int ctas_per_sm_nt() {
-  if (ensure_attrs<NT, false, F8>() != cudaSuccess) return 1;
+  int dev = 0;
+  if (ensure_attrs<NT, false, F8>(&dev) != cudaSuccess) return 1;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (g_ctas_per_sm[NT - 1][F8][dev] > 0) return g_ctas_per_sm[NT - 1][F8][dev];
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Variant<NT, false, F8>::kernel,
                                                     Variant<NT, false, F8>::C::kThreads,
@@ -817,6 +869,8 @@ int ctas_per_sm_nt() {
           cudaSuccess ||
       n < 1)
     return 1;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  g_ctas_per_sm[NT - 1][F8][dev] = n;
   return n;
 }
 
@@ -871,7 +925,10 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
     return cluster_merge ? launch_nt<2, true, true>(k_map, v_map, a, stream)
                          : launch_nt<2, false, true>(k_map, v_map, a, stream);
   }
-  if (deep_grid(false, static_cast<int64_t>(a.num_splits) * a.num_kv_heads * a.batch)) {
+  const int64_t ctas = a.items != nullptr
+                           ? a.item_slots
+                           : static_cast<int64_t>(a.num_splits) * a.num_kv_heads * a.batch;
+  if (deep_grid(false, ctas)) {
     if (a.rows <= 8)
       return cluster_merge ? launch_nt<1, true, false, true>(k_map, v_map, a, stream)
                            : launch_nt<1, false, false, true>(k_map, v_map, a, stream);

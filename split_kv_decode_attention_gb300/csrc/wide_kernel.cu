@@ -74,7 +74,7 @@ constexpr int kWStageBytes = 4 * kWHalf;     // operand stage: K halves, then V 
 constexpr int kWF8Tile = kTileTokens * 128;  // one FP8 tile (K or V): 16 rows of 128 bytes
 // Requests whose schedule tables fit in shared memory (else one item per
 // CTA), and up to which the partial chunks are sorted by length.
-constexpr int kWMaxSchedBatch = 1024;
+constexpr int kWMaxSchedBatch = kWideMaxPlannedBatch;
 constexpr int kWSortBatch = 256;
 // m, l (fp32 probabilities: the LSE) and lq (the same probabilities rounded
 // to the 16-bit P operand: normalises O) per group and row; ok per group
@@ -137,13 +137,12 @@ struct Item {
   int b, kvh, split, L, nsplit, t_begin, t_end, n_tiles, n_iters;
 };
 
-__device__ __forceinline__ Item make_item(const SplitArgs& a, int b, int kvh, int split, int L) {
+__device__ __forceinline__ Item make_item(int chunk, int b, int kvh, int split, int L) {
   Item it;
   it.b = b;
   it.kvh = kvh;
   it.split = split;
   it.L = L;
-  const int chunk = a.chunk_len;
   it.nsplit = L > 0 ? (L + chunk - 1) / chunk : 1;
   it.t_begin = split * chunk;
   it.t_end = min(L, it.t_begin + chunk);
@@ -158,8 +157,13 @@ __device__ __forceinline__ Item make_item(const SplitArgs& a, int b, int kvh, in
 constexpr int kWSchLen = 0;
 constexpr int kWSchFpre = kWMaxSchedBatch;
 constexpr int kWSchPord = 2 * kWMaxSchedBatch + 1;
-constexpr int kWSchTot = 3 * kWMaxSchedBatch + 1;  // full pairs, partial pairs, own length
+constexpr int kWSchTot = 3 * kWMaxSchedBatch + 1;  // full pairs, partial pairs
 constexpr int kWSchRem = 3 * kWMaxSchedBatch + 4;
+// one item per CTA: its request's clamped length, in the space of the
+// unused length table (the item itself is the block index)
+constexpr int kWSchOwnLen = kWSchLen;
+// the call's chunk length (from the params, or the device planner's output)
+constexpr int kWSchChunk = 3 * kWMaxSchedBatch + 3;
 
 // Item k of this CTA. Persistent launch: position k * G + (c or G-1-c,
 // alternating: snake order) in the list where pair p < F is the p-th full
@@ -167,9 +171,10 @@ constexpr int kWSchRem = 3 * kWMaxSchedBatch + 4;
 // pord[i] (partial or empty); kv heads are innermost, so position = pair *
 // Hkv + kvh. Otherwise the block's own item (k = 0 only).
 __device__ __forceinline__ bool schedule_item(const int* sch, const SplitArgs& a, int k, Item* it) {
+  const int chunk = sch[kWSchChunk];
   if (!a.persistent) {
     if (k > 0) return false;
-    *it = make_item(a, blockIdx.z, blockIdx.y, blockIdx.x, sch[kWSchTot + 2]);
+    *it = make_item(chunk, blockIdx.z, blockIdx.y, blockIdx.x, sch[kWSchOwnLen]);
     return true;
   }
   const int G = static_cast<int>(gridDim.x);
@@ -192,9 +197,9 @@ __device__ __forceinline__ bool schedule_item(const int* sch, const SplitArgs& a
   } else {
     b = sch[kWSchPord + pair - F];
     const int L = sch[kWSchLen + b];
-    split = L > 0 ? (L - 1) / a.chunk_len : 0;
+    split = L > 0 ? (L - 1) / chunk : 0;
   }
-  *it = make_item(a, b, kvh, split, sch[kWSchLen + b]);
+  *it = make_item(chunk, b, kvh, split, sch[kWSchLen + b]);
   return true;
 }
 
@@ -230,8 +235,12 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
   const bool persistent = a.persistent != 0;
 
   grid_dependency_wait();
-  // persistent: the first request length of this thread, loaded before the
-  // barrier and TMEM set-up so its latency overlaps them
+  // device-planned call (always persistent): the chunk length from the
+  // planner's output; persistent: the first request length of this thread --
+  // both loaded before the barrier and TMEM set-up so their latency overlaps
+  // them
+  const bool listed = a.items != nullptr;
+  const int chunk = listed ? a.plan[0] : a.chunk_len;
   const int L_first = persistent && tid < a.batch ? a.seq_lens[tid] : 0;
 
   int L0 = 0;  // one item per CTA: its request's clamped length
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     if (a.causal && L > 0 && L < a.q_len) bad |= DA_STATUS_SHORT_CAUSAL;
     if (bad && a.status != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
       atomicOr(a.status, static_cast<int32_t>(bad));
-    const int nsplit = L > 0 ? (L + a.chunk_len - 1) / a.chunk_len : 1;
+    const int nsplit = L > 0 ? (L + chunk - 1) / chunk : 1;
     if (static_cast<int>(blockIdx.x) >= nsplit) return;  // before any TMEM is allocated
     L0 = L;
   }
@@ -294,7 +303,8 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     mbar_init(q_empty, 4);
     mbar_init(item_go, 8);
     fence_mbar_init();
-    s_tot[2] = L0;
+    if (!persistent) sched[kWSchOwnLen] = L0;
+    sched[kWSchChunk] = chunk;
   }
   if (warp == C::kMmaWarp) {
     tmem_alloc(tmem_slot, kWTmemCols);
@@ -303,7 +313,6 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
 
   // ---- schedule tables (persistent launch): clamped lengths, full chunks
   // per request (scanned by warp 0), partial chunks ordered longest first
-  const int chunk = a.chunk_len;
   if (persistent) {
     for (int b = tid; b < a.batch; b += C::kThreads) {
       int L = b == tid ? L_first : a.seq_lens[b];
@@ -313,7 +322,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         L = L < 0 ? 0 : a.max_seq_len;
       }
       if (a.causal && L > 0 && L < a.q_len) bad |= DA_STATUS_SHORT_CAUSAL;
-      if (bad && a.status != nullptr && blockIdx.x == 0)
+      if (bad && a.status != nullptr && blockIdx.x == 0 && !listed)  // (listed: the planner)
         atomicOr(a.status, static_cast<int32_t>(bad));
       s_len[b] = L;
       const int n = L > 0 ? (L + chunk - 1) / chunk : 1;
@@ -867,6 +876,13 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     const int t = r < a.rows ? r / a.group : 0;
     const int h = it.kvh * a.group + (r - t * a.group);
     const int64_t prow = (static_cast<int64_t>(it.b) * a.q_len + t) * a.num_q_heads + h;
+    // partial slot of this row: by item for a device-planned call (item =
+    // pre[b] * Hkv + kvh * n_b + chunk), else by (row, chunk)
+    const int64_t pidx =
+        direct ? 0
+        : listed ? (static_cast<int64_t>(a.pre[it.b]) * a.num_kv_heads +
+                    static_cast<int64_t>(it.kvh) * it.nsplit + it.split) * a.rows + r
+                 : prow * S + it.split;
     // (O is read out here, before this thread's next arrival on item_go lets
     // the next item's P.V overwrite it)
     // both buffers are read unconditionally (a buffer this item did not
@@ -893,7 +909,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
                 make_uint4(pack_bf16x2(o[i], o[i + 1]), pack_bf16x2(o[i + 2], o[i + 3]),
                            pack_bf16x2(o[i + 4], o[i + 5]), pack_bf16x2(o[i + 6], o[i + 7]));
         } else {
-          float* dst = a.part_o + (prow * S + it.split) * kHeadDim + d0;
+          float* dst = a.part_o + pidx * kHeadDim + d0;
           const uint64_t keep = l2_evict_last_policy();
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
@@ -906,7 +922,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       if (direct)
         a.lse[prow] = lse;
       else
-        st_global_hint(a.part_lse + prow * S + it.split, lse, l2_evict_last_policy());
+        st_global_hint(a.part_lse + pidx, lse, l2_evict_last_policy());
     }
     if (!ok) break;
   }
@@ -948,8 +964,13 @@ cudaError_t launch_wide_t(const CUtensorMap& k_map, const CUtensorMap& v_map, co
   SplitArgs pa = a;
   pa.persistent = a.batch <= kWMaxSchedBatch ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  // persistent: one CTA per SM (at most one per possible item)
-  const int64_t items = static_cast<int64_t>(a.num_splits) * a.num_kv_heads * a.batch;
+  // persistent: one CTA per SM (at most one per possible item); otherwise one
+  // CTA per item.  Device-planned calls (batch <= kWMaxSchedBatch, checked by
+  // the host) are always persistent.
+  const bool listed = a.items != nullptr;
+  if (listed && !pa.persistent) return cudaErrorInvalidValue;
+  const int64_t items = listed ? a.item_slots
+                               : static_cast<int64_t>(a.num_splits) * a.num_kv_heads * a.batch;
   cfg.gridDim = pa.persistent ? dim3(static_cast<unsigned>(std::min<int64_t>(sms, items)))
                               : dim3(a.num_splits, a.num_kv_heads, a.batch);
   cfg.blockDim = dim3(WCfg<F8>::kThreads);
@@ -972,12 +993,21 @@ cudaError_t launch_wide(const CUtensorMap& k_map, const CUtensorMap& v_map, cons
 }
 
 int wide_ctas_per_sm() {
+  static int cached[64];  // per device, queried once
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   if (ensure_wide_attrs<false>(nullptr) != cudaSuccess) return 1;
+  {
+    std::lock_guard<std::mutex> lk(g_wide_mu);
+    if (cached[dev] > 0) return cached[dev];
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wide_kernel<false>, WCfg<false>::kThreads,
                                                     WCfg<false>::kSmemBytes) != cudaSuccess ||
       n < 1)
     return 1;
+  std::lock_guard<std::mutex> lk(g_wide_mu);
+  cached[dev] = n;
   return n;
 }
 

@@ -146,6 +146,18 @@ FP8_WORKLOADS = {
 WORKLOADS.update(FP8_WORKLOADS)
 
 
+# Profiling stand-ins: the c3 recipe (same seed, length mix, paging) with 16 of
+# its 64 requests (~1.1 GB of K/V instead of 4.4 GB), so a multi-pass ncu
+# capture of its launch stays within a few GB of device memory; its DRAM
+# traffic per launch scales to c3 by the K/V bytes.
+PROFILE_WORKLOADS = {
+    "c3q_b16_h32kv8_L512-32768_paged": DecodeShape(
+        "c3q_b16_h32kv8_L512-32768_paged", batch=16, q_len=1, num_q_heads=32,
+        num_kv_heads=8, seq_len_lo=512, seq_len_hi=32768, paged=True, seed=1003),
+}
+WORKLOADS.update(PROFILE_WORKLOADS)
+
+
 @dataclasses.dataclass
 class DecodeInputs:
     """Host (numpy) or device (torch) arrays of one workload instance.

@@ -83,3 +83,18 @@ def test_reference_arm_prints_the_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_default_run_times_every_gate_workload_with_c3_as_headline():
+    """The default bench covers the five gate workloads; the headline is the
+    largest single-GPU one (c3), and the reference arm follows it."""
+    import bench
+    from split_kv_decode_attention_gb300 import workloads as W
+    args = bench.parse_args([])
+    assert args.workload == bench.DEFAULT_WORKLOAD
+    assert bench.HEADLINE_WORKLOAD in bench.GATE_WORKLOADS
+    assert bench.GATE_WORKLOADS == W.WORKLOAD_ORDER   # the five workload recipes
+    lens = {n: W.draw_seq_lens(W.WORKLOADS[n], __import__("numpy").random.default_rng(
+        W.WORKLOADS[n].seed)) for n in bench.GATE_WORKLOADS}
+    kv = {n: int(lens[n].sum()) * W.WORKLOADS[n].num_kv_heads for n in lens}
+    assert max(kv, key=kv.get) == bench.HEADLINE_WORKLOAD
