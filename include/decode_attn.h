@@ -103,12 +103,15 @@ extern "C" {
                                       cluster merge); needed to read partials */
 #define DA_FLAG_KV_FP8_E4M3 2u     /* K and V caches are FP8 E4M3 bytes scaled by
                                       k_scale / v_scale (see "FP8 caches" above) */
-#define DA_FLAG_TEST_WITHHOLD_COPY 0x100u /* test hook for failure detection: with
-                                      DA_FLAG_TWO_PASS and at most 16 rows per kv
-                                      head, block (0, 0, 0) of the split launch never
-                                      fills its first pipeline stage, so its bounded
-                                      wait runs out (~2 s) and DA_STATUS_TIMEOUT is
-                                      set; no fault, the context stays usable */
+#define DA_FLAG_TEST_WITHHOLD_COPY 0x100u /* test hook for failure detection:
+                                      block (0, 0, 0) of the split launch never
+                                      fills its first pipeline stage (at most 16
+                                      rows per kv head: with DA_FLAG_TWO_PASS; above
+                                      16, the tcgen05 kernel: the first stage of
+                                      its first work item), so the bounded waits
+                                      on it run out (~2 s each) and
+                                      DA_STATUS_TIMEOUT is set; no fault, the
+                                      context stays usable */
 
 /* device status bits (OR-ed into *status) */
 #define DA_STATUS_BAD_PAGE 1u      /* block-table entry outside [0, num_pages) */

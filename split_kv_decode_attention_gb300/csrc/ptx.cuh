@@ -79,15 +79,22 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
-// Wait for the phase with the given parity to complete; false on time-out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after
+// limit_ns (or 2^30 polls) without it.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1; i < (1u << 30); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 31u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
   return false;
+}
+
+// Wait for the phase with the given parity to complete; false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA

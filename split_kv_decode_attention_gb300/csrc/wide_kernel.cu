@@ -77,8 +77,8 @@ constexpr int kWF8Tile = kTileTokens * 128;  // one FP8 tile (K or V): 16 rows o
 constexpr int kWMaxSchedBatch = kWideMaxPlannedBatch;
 constexpr int kWSortBatch = 256;
 // m, l (fp32 probabilities: the LSE) and lq (the same probabilities rounded
-// to the 16-bit P operand: normalises O) per group and row; ok per group
-constexpr int kWStatFloats = 6 * kWRows + 2;
+// to the 16-bit P operand: normalises O) per group and row; ok per softmax warp
+constexpr int kWStatFloats = 6 * kWRows + 8;
 constexpr int kWStatBytes = 3200;
 constexpr int kWSchedInts = 4 * kWMaxSchedBatch + 4;
 static_assert(kWStatFloats * 4 <= kWStatBytes, "statistics buffer");
@@ -116,8 +116,8 @@ struct WCfg {
   static constexpr int kOffBar = kOffSched + ((kWSchedInts * 4 + 15) & ~15);
   // full[], empty[] of the TMA ring, conv_full[], conv_empty[] of the operand
   // ring (FP8), then s_full, s_free, p_full, pv_done per group, q_full,
-  // q_empty, item_go
-  static constexpr int kNumBars = 2 * kStages + (F8 ? 2 * kOpStages : 0) + 8 + 3;
+  // q_empty, item_go, grp_sync, tmem_done
+  static constexpr int kNumBars = 2 * kStages + (F8 ? 2 * kOpStages : 0) + 8 + 5;
   static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
   static_assert(kProducers >= 1 && kBoxes <= 32 * kProducers, "one box per producer lane");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -274,6 +274,8 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
   uint64_t* q_full = pv_done + 2;              // Q rows of the next item staged
   uint64_t* q_empty = q_full + 1;              // staging copied into TMEM
   uint64_t* item_go = q_empty + 1;             // Q in TMEM, previous outputs read (items with keys)
+  uint64_t* grp_sync = item_go + 1;            // both softmax groups' statistics written (per item)
+  uint64_t* tmem_done = grp_sync + 1;          // softmax warps are done with TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   int* sched = reinterpret_cast<int*>(smem + C::kOffSched);
   int* s_len = sched + kWSchLen;
@@ -302,6 +304,8 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     mbar_init(q_full, 32 * C::kProducers);
     mbar_init(q_empty, 4);
     mbar_init(item_go, 8);
+    mbar_init(grp_sync, 8);
+    mbar_init(tmem_done, 8);
     fence_mbar_init();
     if (!persistent) sched[kWSchOwnLen] = L0;
     sched[kWSchChunk] = chunk;
@@ -406,6 +410,11 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     int gs = 0;       // stages of all previous items
     int last_g = -1;  // the last stage this warp issued
     bool ok = true;
+    // test hook (DA_FLAG_TEST_WITHHOLD_COPY): CTA 0 never fills the first
+    // stage of its first item, so the waits on it run out and report
+    // DA_STATUS_TIMEOUT
+    const bool withhold =
+        a.test_withhold != 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
     // token -> (page, slot): shifts when the page size is a power of two (the
     // bf16 producers issue 16 boxes a stage and their instruction count sets
     // the stage pace: w64 226 -> 215 us; the FP8 variant keeps the division)
@@ -474,9 +483,10 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         pg_next = page_of(i + 1);
         const bool last = i == it.n_iters - 1;
         const int boxes = last ? last_boxes : C::kBoxes;  // boxes with data
-        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], last ? last_bytes : full_bytes);
+        const bool skip = withhold && gs + i == 0;
+        if (lane == 0 && !skip) mbar_arrive_expect_tx(&full_bar[s], last ? last_bytes : full_bytes);
         __syncwarp();
-        if (bx < boxes) {
+        if (bx < boxes && !skip) {
           if (a.paged && static_cast<unsigned>(pg) >= static_cast<unsigned>(a.num_pages)) {
             if (a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_BAD_PAGE));
             pg = 0;
@@ -502,7 +512,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       if (!ok && a.status != nullptr) atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
       // no copy of this warp may still be landing when the CTA exits
       for (int g = max(0, last_g - C::kStages + 1); g <= last_g; ++g)
-        mbar_wait(&full_bar[g % C::kStages], (g / C::kStages) & 1);
+        if (!(withhold && g == 0)) mbar_wait(&full_bar[g % C::kStages], (g / C::kStages) & 1);
     }
     return;
   }
@@ -672,10 +682,16 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       u0 += (n + 1) >> 1;
       u1 += n >> 1;
     }
+    // TMEM is released once the softmax warps are done with it.  Each of
+    // their waits gives up after kWaitLimitNs, and after a failure a softmax
+    // warp passes at most two more waits (its group's statistics exchange and
+    // this arrival) before arriving here, so kTmemDoneWaits limits cover it
+    // with room to spare; should even that run out, TMEM is released anyway
+    // (a CTA that kept it would block the next allocation on this SM).
+    constexpr unsigned long long kTmemDoneWaits = 5;
+    ok = (__all_sync(kFull, mbar_wait_for(tmem_done, 0, kTmemDoneWaits * kWaitLimitNs)) != 0) && ok;
     if (!ok && lane == 0 && a.status != nullptr)
       atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
-    __syncwarp();
-    named_barrier_sync(3, kWSoftmaxThreads + 32);  // softmax warps are done with TMEM
     tc_fence_after_sync();
     tmem_dealloc(tmem, kWTmemCols);
     return;
@@ -850,16 +866,28 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     // ---- merge the two groups (same recurrence as the combine) and write
     // O / l (final bf16 row or fp32 partial) and the LSE; group g writes the
     // d-columns [64 g, 64 g + 64) of every row
+    // The exchange needs one barrier per item: the buffer (k & 1) was last
+    // read before item k - 1's barrier, which every writer has passed; the
+    // barrier also orders both groups' last P.V (each waited for its own)
+    // before either reads the other's O columns.  It is an mbarrier (one
+    // arrival per warp) with a bounded wait; a warp whose wait runs out
+    // reports it through the flags and the item loop ends.
     float* stat = reinterpret_cast<float*>(smem + C::kOffStat + (k & 1) * kWStatBytes);
-    tc_fence_before_sync();
-    named_barrier_sync(4, kWSoftmaxThreads);  // both groups' last P.V are done
     stat[grp * 384 + r] = m_used;
     stat[grp * 384 + 128 + r] = l;
     stat[grp * 384 + 256 + r] = lq;
-    if (tid == grp * 128) stat[768 + grp] = ok ? 1.f : 0.f;
-    named_barrier_sync(4, kWSoftmaxThreads);
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+      stat[768 + warp] = ok ? 1.f : 0.f;
+      mbar_arrive(grp_sync);
+    }
+    const bool synced = __all_sync(kFull, mbar_wait(grp_sync, k & 1)) != 0;
     tc_fence_after_sync();
-    ok = stat[768] != 0.f && stat[769] != 0.f;  // the same for all 256 threads
+    ok = synced;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) ok = ok && stat[768 + w] != 0.f;  // (all 256 threads agree
+                                                                  //  unless a wait ran out)
     const float m0 = stat[r], l0 = stat[128 + r], q0 = stat[256 + r];
     const float m1 = stat[384 + r], l1 = stat[512 + r], q1 = stat[640 + r];
     const float M = fmaxf(m0, m1);
@@ -929,7 +957,8 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
   if (!ok && lane == 0 && a.status != nullptr)
     atomicOr(a.status, static_cast<int32_t>(DA_STATUS_TIMEOUT));
   tc_fence_before_sync();
-  named_barrier_sync(3, kWSoftmaxThreads + 32);  // the MMA warp releases TMEM after this
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tmem_done);  // the MMA warp releases TMEM after all 8
 }
 
 std::mutex g_wide_mu;

@@ -370,3 +370,35 @@ def test_withheld_copy_times_out_and_context_stays_usable(binding):
     ref_o, ref_l = oracle.decode_attention_inputs(inp)
     assert_out_close(bf16_tensor_to_f64(out), ref_o)
     assert_lse_close(lse.cpu().numpy(), ref_l)
+
+
+def test_withheld_copy_times_out_in_the_tcgen05_kernel_and_context_stays_usable(binding):
+    """The same failure detection on the tcgen05 kernel (64 rows per KV head):
+    CTA 0 never fills the first stage of its first work item, so the MMA
+    warp's idle limit and the softmax warps' bounded waits run out, the
+    groups' statistics exchange and the TMEM release wait on bounded
+    mbarriers, and the call reports DA_STATUS_TIMEOUT; the next call on the
+    same context is exact."""
+    import time
+    shp = W.small_shape("withhold_wide", batch=2, q_len=8, num_q_heads=16, num_kv_heads=2,
+                        lo=500, hi=900, causal=True, seed=71)
+    inp = W.make_host_inputs(shp)
+    q, k, v, bt, lens = to_device(inp)
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True,
+                                    two_pass=True)
+    p.flags |= binding.DA_FLAG_TEST_WITHHOLD_COPY
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len, causal=True,
+                        num_splits=2, status=status, params=p)
+    torch.cuda.synchronize()
+    assert int(status.item()) & binding.DA_STATUS_TIMEOUT
+    assert time.time() - t0 < 60
+    status.zero_()
+    out, lse = binding.decode_attn(q, k, v, bt, lens, max_seq_len=inp.max_seq_len, causal=True,
+                                   num_splits=2, status=status, two_pass=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle.decode_attention_inputs(inp)
+    assert_out_close(bf16_tensor_to_f64(out), ref_o)
+    assert_lse_close(lse.cpu().numpy(), ref_l)
