@@ -158,7 +158,10 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
   return plan_for_slots(p, host_seq_lens, slots, num_splits, chunk_len);
 }
 
-int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p, bool paged) {
+// box_tokens: token rows per box (16; a whole stage for contiguous caches
+// on the warp-MMA kernel)
+int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p, bool paged,
+                int box_tokens) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return DA_ERR_CUDA;
   // dims, innermost first: d (128), kv head, token-in-group, group
@@ -176,7 +179,7 @@ int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p,
                                  static_cast<cuuint64_t>(p->kv_stride_token) * eb,
                                  static_cast<cuuint64_t>(p->kv_stride_page) * eb};
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 1,
-                             static_cast<cuuint32_t>(kTileTokens), 1};
+                             static_cast<cuuint32_t>(box_tokens), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, kv_fp8(p) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    4, const_cast<void*>(base), dims, strides, box, estr,
@@ -447,13 +450,18 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
       return DA_ERR_WORKSPACE;
   }
 
+  // the split launch's grid (it picks the pipeline shape, and with it the box
+  // height for contiguous caches)
+  const int64_t ctas =
+      listed ? lay.cap : static_cast<int64_t>(eff) * p->num_kv_heads * p->batch;
+  const int box_tokens = dattn::split_box_tokens(rows_of(p), kv_fp8(p), paged, ctas);
   CUtensorMap kmap, vmap;
   std::memset(&kmap, 0, sizeof(kmap));
   std::memset(&vmap, 0, sizeof(vmap));
   if (!no_keys) {
-    rc = make_kv_map(&kmap, k_cache, p, paged);
+    rc = make_kv_map(&kmap, k_cache, p, paged, box_tokens);
     if (rc != DA_OK) return rc;
-    rc = make_kv_map(&vmap, v_cache, p, paged);
+    rc = make_kv_map(&vmap, v_cache, p, paged, box_tokens);
     if (rc != DA_OK) return rc;
   }
 
@@ -492,6 +500,8 @@ int run_decode(const decode_attn_params* p, const void* q, const void* k_cache,
   a.kv_fp8 = kv_fp8(p) ? 1 : 0;
   a.test_withhold = (p->flags & DA_FLAG_TEST_WITHHOLD_COPY) != 0 ? 1 : 0;
   a.v_scale = kv_fp8(p) ? p->v_scale : 1.f;
+  // (no keys: no tensor map was encoded and no copy may be issued)
+  a.big_box = box_tokens > kTileTokens && !no_keys ? 1 : 0;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(workspace);

@@ -38,6 +38,7 @@ struct SplitArgs {
   int kv_fp8;                          // caches hold FP8 E4M3
   float v_scale;                       // FP8: values = v_scale * V (k_scale is in scale_log2)
   int test_withhold;                   // DA_FLAG_TEST_WITHHOLD_COPY (narrow kernel, two-pass)
+  int big_box;                         // contiguous caches: the maps' boxes span a whole stage
   // Device-planned calls (items != nullptr): the planner kernel wrote the
   // chunk length and item count to plan[0..1], per-request prefixes of chunk
   // counts to pre[], and the work items (b, kv head, chunk, clamped length) to
@@ -123,6 +124,11 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
 // True when clusters of num_splits CTAs (2..16) are supported and the device
 // can hold num_clusters of them at once (one wave).
 bool split_cluster_merge_fits(int rows, bool fp8, int num_splits, int64_t num_clusters);
+
+// Token rows of the TMA boxes the split launch expects: a whole stage (16 x
+// tiles per stage) for contiguous caches on the warp-MMA kernel, else 16.
+// `ctas` is the launch's grid size (it picks the pipeline shape).
+int split_box_tokens(int rows, bool fp8, bool paged, int64_t ctas);
 
 // Resident split CTAs per SM for the kernel variant serving `rows` rows.
 int split_ctas_per_sm(int rows, bool fp8);

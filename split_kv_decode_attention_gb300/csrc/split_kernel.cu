@@ -65,6 +65,14 @@ struct SplitCfg {
   // one 16-token K (or V) tile: two bf16 halves, or 16 rows of 128 FP8 bytes
   static constexpr int kTileBytes = F8 ? kTileTokens * 128 : 2 * kHalfBytes;
   static constexpr int kStageBytes = 2 * TPS * kTileBytes;  // TPS K tiles, then TPS V tiles
+  // Inside the K (or V) region of a stage the layout is d-half-major: the
+  // 128-byte rows of the TPS tiles' first 64 d (bf16), then of their last 64
+  // d -- [2 halves][16 TPS tokens][128 B] -- so one TMA box of 16 TPS tokens
+  // fills a whole half (contiguous caches) and 16-token boxes (paged caches)
+  // land in the same place.  FP8 tiles are whole 128-byte rows already.
+  static constexpr int kRegionBytes = TPS * kTileBytes;    // K (or V) of a stage
+  static constexpr int kTileStride = kTileTokens * 128;    // next tile, same d-half
+  static constexpr int kHalfStride = F8 ? 0 : TPS * kTileStride;  // next d-half
   static constexpr int kPipeBytes = STAGES * kStageBytes;
   static constexpr int kRows = 8 * NT;                     // padded query rows
   static constexpr int kRedStride = kHeadDim + 4;          // floats per row (bank spread)
@@ -83,14 +91,25 @@ struct SplitCfg {
   static constexpr int kQBytes = kQSmem ? kRows * 256 : 0;
   static constexpr int kBarBytes = 2 * STAGES * 8;
   static constexpr int kStatBytes = 3 * TPS * kRows * 4 + kRows * 4;
-  static constexpr int kSmemBytes = 1024 + kPipeBytes + kQBytes + kBarBytes + kStatBytes;
+  // Cluster merge of the deep bf16 shape (4 tiles per stage; it runs at most
+  // one CTA per SM, so shared memory is plentiful): every CTA pushes its
+  // merged (row, 4 d) units and their rows' LSEs into the inbox of the CTA
+  // that owns each unit.  Unit u of U = rows x 32 goes to CTA u mod S, slot
+  // u / S, so an inbox holds S x ceil(U / S) <= U + 15 entries per array.
+  static constexpr bool kPushMerge = TPS == 4 && !F8;
+  static constexpr int kInboxUnits = kRows * 32 + 16;
+  static constexpr int kOffInbox = (kPipeBytes + kQBytes + kBarBytes + kStatBytes + 15) / 16 * 16;
+  static constexpr int kInboxBytes = kPushMerge ? kInboxUnits * (16 + 4) : 0;
+  static constexpr int kSmemBytes = 1024 + kOffInbox + kInboxBytes;
 };
 
 // Byte address of 16-byte chunk `chunk` (0..15, i.e. d = 8*chunk) of token row
-// `tok` inside one tile: two 2048-byte halves [16 tokens][64 d], 128-byte rows,
-// chunk index XOR-ed with (tok & 7) as the TMA 128-byte swizzle lays it out.
-__device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int tok, int chunk) {
-  return tile + ((chunk >> 3) << 11) + (tok << 7) + (((chunk & 7) ^ (tok & 7)) << 4);
+// `tok` inside one bf16 tile: d-half chunk / 8 at half_stride bytes per half,
+// 128-byte rows, chunk index XOR-ed with (tok & 7) as the TMA 128-byte swizzle
+// lays it out (every half starts on a 1024-byte boundary).
+__device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int tok, int chunk,
+                                              uint32_t half_stride) {
+  return tile + (chunk >> 3) * half_stride + (tok << 7) + (((chunk & 7) ^ (tok & 7)) << 4);
 }
 
 __device__ __forceinline__ uint32_t load_u32(const uint16_t* p) {
@@ -132,7 +151,12 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     split = blockIdx.x;
     kvh = blockIdx.y;
     b = blockIdx.z;
-    L = a.seq_lens[b];
+    L = a.seq_lens[b];  // (under the cluster merge its load overlaps the set-up)
+    chunk = a.chunk_len;
+  }
+  // the request length, clamped, with its status bits (grid-planned calls)
+  auto take_length = [&]() {
+    if (listed) return;
     uint32_t bad = 0;
     if (L < 0 || L > a.max_seq_len) {
       bad |= DA_STATUS_SEQ_LEN;
@@ -141,15 +165,14 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     if (a.causal && L > 0 && L < a.q_len) bad |= DA_STATUS_SHORT_CAUSAL;
     if (bad && a.status != nullptr && split == 0 && kvh == 0 && threadIdx.x == 0)
       atomicOr(a.status, static_cast<int32_t>(bad));
-    chunk = a.chunk_len;
+  };
+  if constexpr (!CM) {
+    // a CTA past its request's chunks exits before any set-up (with the
+    // cluster merge every CTA stays: an empty chunk contributes 0 / -inf)
+    take_length();
+    if (split >= (L > 0 ? (L + chunk - 1) / chunk : 1)) return;
   }
-  const int nsplit_b = L > 0 ? (L + chunk - 1) / chunk : 1;
-  // (with the cluster merge every CTA stays: an empty chunk contributes 0 / -inf)
-  if (!CM && split >= nsplit_b) return;
   const int t_begin = split * chunk;
-  const int t_end = min(L, t_begin + chunk);
-  const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTileTokens - 1) / kTileTokens : 0;
-  const int n_iters = (n_tiles + TPS - 1) / TPS;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -161,6 +184,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
   float* stat_l = stat_m + TPS * C::kRows;
   float* stat_q = stat_l + TPS * C::kRows;
   float* xl = stat_q + TPS * C::kRows;  // cluster merge: this CTA's per-row LSE
+  float4* inbox_v = reinterpret_cast<float4*>(smem + C::kOffInbox);  // (push merge)
+  float* inbox_l = reinterpret_cast<float*>(smem + C::kOffInbox + C::kInboxUnits * 16);
 
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -171,10 +196,41 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     fence_mbar_init();
   }
   __syncthreads();
+  // push merge: the first phase of the cluster barrier, waited on just
+  // before the pushes (every peer has started by then)
+  if constexpr (CM && C::kPushMerge) cluster_arrive_relaxed();
+
+  // Cluster merge with a contiguous cache: the first stage is one box per (K
+  // or V, d-half) from t_begin, which does not depend on the request length,
+  // so the producer issues it while the length's load is still in flight (a
+  // chunk that turns out empty or short just leaves some of it unused; the
+  // producer still waits for it before leaving).  (t_begin < max_seq_len for
+  // every chunk of the grid, so the box starts inside the cache.)
+  const bool early = CM && a.big_box != 0;
+  if (CM && early && warp == TPS) {
+    if (lane == 0) {
+      prefetch_tensor_map(&k_map);
+      prefetch_tensor_map(&v_map);
+      mbar_arrive_expect_tx(&full_bar[0], static_cast<uint32_t>(C::kStageBytes));
+    }
+    __syncwarp();
+    if (lane < (F8 ? 2 : 4)) {
+      const bool is_v = F8 ? (lane & 1) != 0 : (lane & 2) != 0;
+      const int half = F8 ? 0 : lane & 1;
+      tma_load_4d(smem + (is_v ? C::kRegionBytes : 0) + half * C::kHalfStride,
+                  is_v ? &v_map : &k_map, &full_bar[0], half * 64, kvh, t_begin, b,
+                  l2_evict_first_policy());
+    }
+  }
+  if constexpr (CM) take_length();
+  const int nsplit_b = L > 0 ? (L + chunk - 1) / chunk : 1;
+  const int t_end = min(L, t_begin + chunk);
+  const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTileTokens - 1) / kTileTokens : 0;
+  const int n_iters = (n_tiles + TPS - 1) / TPS;
 
   // =========================================================== producer warp
   if (warp == TPS) {
-    if (lane == 0) {
+    if (lane == 0 && !early) {
       prefetch_tensor_map(&k_map);
       prefetch_tensor_map(&v_map);
     }
@@ -183,11 +239,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     // physical page of tile (it * TPS + lane); fetched one stage ahead
     PageWindow pw{bt_row, t_begin, n_tiles, a.page_size, a.num_pages, lane, a.status, 0, 0, 0};
     if (a.paged) pw.init();
-    int issued = 0;
+    int issued = early ? 1 : 0;  // (the early first stage)
     bool ok = true;
     const bool withhold =
         a.test_withhold != 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
-    for (int it = 0; it < n_iters; ++it) {
+    for (int it = issued; it < n_iters; ++it) {
       const int s = it % STAGES;
       const int use = it / STAGES;
       int good = 1;
@@ -214,6 +270,26 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         ++issued;
         continue;
       }
+      uint8_t* stage = smem + s * C::kStageBytes;
+      if (a.big_box) {
+        // contiguous cache: one box of 16 TPS tokens per (K or V, d-half)
+        // fills the whole stage region (the last stage may read tokens past
+        // the chunk, which no consumer uses; past the cache the box is
+        // zero-filled), so its byte count is always the full stage
+        constexpr int kBigBoxes = F8 ? 2 : 4;
+        if (lane == 0) mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(C::kStageBytes));
+        __syncwarp();
+        if (lane < kBigBoxes) {
+          const bool is_v = F8 ? (lane & 1) != 0 : (lane & 2) != 0;
+          const int half = F8 ? 0 : lane & 1;
+          tma_load_4d(stage + (is_v ? C::kRegionBytes : 0) + half * C::kHalfStride,
+                      is_v ? &v_map : &k_map, &full_bar[s], half * 64, kvh,
+                      t_begin + it * TPS * kTileTokens, b, policy);
+        }
+        ++issued;
+        __syncwarp();
+        continue;
+      }
       if (lane == 0)
         mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(tiles_here * 2 * kBoxBytes));
       __syncwarp();
@@ -225,7 +301,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         const int grp = a.paged ? my_pg : b;
         const int tin = a.paged ? tok % a.page_size : tok;
         const bool is_v = (lane & 1) != 0;
-        uint8_t* dst = smem + s * C::kStageBytes + ((is_v ? TPS : 0) + i) * C::kTileBytes;
+        uint8_t* dst = stage + (is_v ? C::kRegionBytes : 0) + i * C::kTileStride;
         tma_load_4d(dst, is_v ? &v_map : &k_map, &full_bar[s], 0, kvh, tin, grp, policy);
       }
       // one TMA box per lane (tile = lane / 4; K or V, d-half from lane % 4)
@@ -236,8 +312,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         const int tin = a.paged ? tok % a.page_size : tok;
         const int half = lane & 1;
         const bool is_v = (lane & 2) != 0;
-        uint8_t* dst = smem + s * C::kStageBytes + ((is_v ? TPS : 0) + i) * C::kTileBytes +
-                       half * C::kHalfBytes;
+        uint8_t* dst = stage + (is_v ? C::kRegionBytes : 0) + half * C::kHalfStride +
+                       i * C::kTileStride;
         tma_load_4d(dst, is_v ? &v_map : &k_map, &full_bar[s], half * 64, kvh, tin, grp, policy);
       }
       ++issued;
@@ -251,8 +327,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         if (!(withhold && it == 0)) mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1);
     }
     if constexpr (CM) {
-      // the consumers' two cluster barriers need every thread of the cluster
-      cluster_sync();
+      // the consumers' two cluster-barrier phases need every thread of the cluster
+      if constexpr (C::kPushMerge) cluster_wait();
+      else cluster_sync();
       cluster_sync();
     }
     return;
@@ -351,8 +428,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     if (!ok) break;
     const int tile = it * TPS + warp;
     if (tile < n_tiles) {
-      const uint32_t kt = smem_base + s * C::kStageBytes + warp * C::kTileBytes;
-      const uint32_t vt = kt + TPS * C::kTileBytes;
+      const uint32_t kt = smem_base + s * C::kStageBytes + warp * C::kTileStride;
+      const uint32_t vt = kt + C::kRegionBytes;
       const int tok0 = t_begin + tile * kTileTokens;
       // ---- S^T[16 keys x 8*NT rows] = K . Q^T
       float sc[NT][4];
@@ -405,7 +482,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           uint32_t af[4];
-          ldsm_x4(tile_addr(kt, (lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)), af);
+          ldsm_x4(tile_addr(kt, (lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4),
+                            C::kHalfStride),
+                  af);
           uint32_t qb[NT][2];
           q_frag(ks, qb);
 #pragma unroll
@@ -462,7 +541,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
       // NaN), so zero those rows of the tile before using it
       if (tok0 + kTileTokens > L) {
         const int first = L - tok0;  // >= 1 since tok0 < t_end <= L
-        uint8_t* vgen = smem + s * C::kStageBytes + (TPS + warp) * C::kTileBytes;
+        uint8_t* vgen = smem + s * C::kStageBytes + C::kRegionBytes + warp * C::kTileStride;
         if constexpr (F8) {  // whole 128-byte rows
           for (int idx = lane; idx < (kTileTokens - first) * 8; idx += 32)
             *reinterpret_cast<uint4*>(vgen + (first + (idx >> 3)) * 128 + (idx & 7) * 16) =
@@ -471,7 +550,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
           for (int idx = lane; idx < (kTileTokens - first) * 16; idx += 32) {
             const int row = first + (idx >> 4);
             const int c = idx & 15;
-            *reinterpret_cast<uint4*>(vgen + ((c >> 3) << 11) + (row << 7) + ((c & 7) << 4)) =
+            *reinterpret_cast<uint4*>(vgen + (c >> 3) * C::kHalfStride + (row << 7) + ((c & 7) << 4)) =
                 make_uint4(0u, 0u, 0u, 0u);
           }
         }
@@ -506,7 +585,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           uint32_t af[4];
-          ldsm_x4_trans(tile_addr(vt, (lane & 7) + (lane >> 4) * 8, 2 * mt + ((lane >> 3) & 1)), af);
+          ldsm_x4_trans(tile_addr(vt, (lane & 7) + (lane >> 4) * 8, 2 * mt + ((lane >> 3) & 1),
+                                  C::kHalfStride),
+                        af);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], af, pb[nt][0], pb[nt][1]);
         }
@@ -548,9 +629,13 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         stat_q[warp * C::kRows + row] = lq[nt][rr];
       }
   }
+  // every consumer warp is done with the stage ring (a warp may still be
+  // reading any of its last stages until then) ...
   named_barrier_sync(1, 32 * TPS);
-
-  float* red = reinterpret_cast<float*>(smem);  // the stage ring is idle now
+  // ... so each warp writes its O rows, scaled by its weight f = e^{m_w - M}
+  // / sum_w lq_w e^{m_w - M} (the rounded-P sums normalise O; v_scale for FP8
+  // caches), into it; after a second barrier the rows of the warps are summed.
+  float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -576,44 +661,105 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     }
   named_barrier_sync(1, 32 * TPS);
 
-  if constexpr (CM) {
-    // ---- cluster merge: publish this CTA's (O, lse), then each CTA of the
-    // cluster reduces a slice of the rows over all CTAs through distributed
-    // shared memory (the same max / weighted-sum merge as the combine kernel)
+  // the row's natural-log LSE from the warps' fp32 sums
+  auto row_lse = [&](int row) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < TPS; ++w) M = fmaxf(M, stat_m[w * C::kRows + row]);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < TPS; ++w)
+      Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
+    return Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -INFINITY;
+  };
+  // the merged (row, d..d+3) of the CTA's output: the warps' scaled rows summed
+  auto merged = [&](int row, int d) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < TPS; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(red + (w * C::kRows + row) * C::kRedStride + d);
+      v.x += x.x;
+      v.y += x.y;
+      v.z += x.z;
+      v.w += x.w;
+    }
+    return v;
+  };
+
+  if constexpr (CM && C::kPushMerge) {
+    // ---- cluster merge by push: every CTA writes each merged (row, 4 d)
+    // unit and its row's LSE into the inbox of the unit's owner (CTA u mod S,
+    // slot u / S); one cluster barrier publishes them, and each owner reduces
+    // its units from its own shared memory (the same max / weighted-sum merge
+    // as the combine kernel) -- no remote loads, no second barrier
+    const int S = gridDim.x;  // cluster = all chunks of this (kv head, request), <= 16
+    const int units = a.rows * 32;
+    const int slots = (units + S - 1) / S;
+    cluster_wait();  // every peer has started: its inbox may be written
+    for (int u = threadIdx.x; u < units; u += 32 * TPS) {
+      const int row = u >> 5;
+      const int owner = u % S;
+      const int slot = u / S;
+      const uint32_t dv = smem_addr(inbox_v + split * slots + slot);
+      const uint32_t dl = smem_addr(inbox_l + split * slots + slot);
+      st_cluster_f32x4(map_to_rank(dv, owner), merged(row, (u & 31) * 4));
+      st_cluster_f32(map_to_rank(dl, owner), row_lse(row));
+    }
+    cluster_sync();  // every push has landed
+    for (int slot = threadIdx.x; slot < slots; slot += 32 * TPS) {
+      const int u = slot * S + split;
+      if (u >= units) break;
+      const int row = u >> 5;
+      const int d = (u & 31) * 4;
+      float M = -INFINITY;
+      for (int r = 0; r < S; ++r) M = fmaxf(M, inbox_l[r * slots + slot]);
+      float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float W = 0.f;
+      if (M != -INFINITY) {
+        for (int r = 0; r < S; ++r) {  // peers in rank order
+          const float w = ex2((inbox_l[r * slots + slot] - M) * kLog2e);
+          const float4 x = inbox_v[r * slots + slot];
+          W += w;
+          acc4.x += w * x.x;
+          acc4.y += w * x.y;
+          acc4.z += w * x.z;
+          acc4.w += w * x.w;
+        }
+      }
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      const int t = row / a.group;
+      const int h = kvh * a.group + (row - t * a.group);
+      *reinterpret_cast<uint2*>(a.out + static_cast<int64_t>(b) * a.o_sb +
+                                static_cast<int64_t>(t) * a.o_st +
+                                static_cast<int64_t>(h) * a.o_sh + d) =
+          make_uint2(pack_bf16x2(acc4.x * inv, acc4.y * inv),
+                     pack_bf16x2(acc4.z * inv, acc4.w * inv));
+      if (d == 0) {
+        const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
+        a.lse[prow] = W > 0.f ? M + logf(W) : -INFINITY;
+      }
+    }
+    return;
+  } else if constexpr (CM) {
+    // ---- cluster merge: publish this CTA's (O, lse), then the CTAs of the
+    // cluster reduce the rows over all CTAs through distributed shared
+    // memory (the same max / weighted-sum merge as the combine kernel)
     float* xo = reinterpret_cast<float*>(smem + C::kXoOffset);
     for (int idx = threadIdx.x; idx < a.rows * 32; idx += 32 * TPS) {
       const int row = idx >> 5;
       const int d = (idx & 31) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < TPS; ++w) {
-        const float4 x =
-            *reinterpret_cast<const float4*>(red + (w * C::kRows + row) * C::kRedStride + d);
-        v.x += x.x;
-        v.y += x.y;
-        v.z += x.z;
-        v.w += x.w;
-      }
-      *reinterpret_cast<float4*>(xo + row * kHeadDim + d) = v;
+      *reinterpret_cast<float4*>(xo + row * kHeadDim + d) = merged(row, d);
     }
-    if (threadIdx.x < a.rows) {
-      const int row = threadIdx.x;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < TPS; ++w) M = fmaxf(M, stat_m[w * C::kRows + row]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float Ls = 0.f;
-#pragma unroll
-      for (int w = 0; w < TPS; ++w)
-        Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
-      xl[row] = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -INFINITY;
-    }
+    if (threadIdx.x < a.rows) xl[threadIdx.x] = row_lse(threadIdx.x);
     cluster_sync();  // every CTA's (O, lse) is visible cluster-wide
 
     const int S = gridDim.x;  // cluster = all chunks of this (kv head, request), <= 16
     const uint32_t xo_addr = smem_addr(xo);
     const uint32_t xl_addr = smem_addr(xl);
-    for (int u = split * 32 * TPS + threadIdx.x; u < a.rows * 32; u += S * 32 * TPS) {
+    // (row, 4 d) units interleaved over the CTAs of the cluster (unit u goes
+    // to CTA u mod S), so every CTA reduces an equal share
+    for (int u = threadIdx.x * S + split; u < a.rows * 32; u += 32 * TPS * S) {
       const int row = u >> 5;
       const int d = (u & 31) * 4;
       // every peer's LSE and the first 8 peers' output slices in one round
@@ -646,7 +792,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
           }
 #pragma unroll
           for (int j = 0; j < kHalf; ++j) {
-            if (r0 + j < S) {  // peers in rank order: the sums of the earlier form
+            if (r0 + j < S) {  // peers in rank order
               const float w = ex2((lr[r0 + j] - M) * kLog2e);
               W += w;
               acc4.x += w * x[j].x;
@@ -673,20 +819,12 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     cluster_sync();  // no CTA leaves while another may still read its smem
     return;
   } else {
-  const bool direct = nsplit_b == 1;
+    const bool direct = nsplit_b == 1;
     const int S = a.num_splits;
     for (int idx = threadIdx.x; idx < a.rows * 32; idx += 32 * TPS) {
       const int row = idx >> 5;
       const int d = (idx & 31) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < TPS; ++w) {
-        const float4 x = *reinterpret_cast<const float4*>(red + (w * C::kRows + row) * C::kRedStride + d);
-        v.x += x.x;
-        v.y += x.y;
-        v.z += x.z;
-        v.w += x.w;
-      }
+      const float4 v = merged(row, d);
       const int t = row / a.group;
       const int h = kvh * a.group + (row - t * a.group);
       if (direct) {
@@ -703,15 +841,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     }
     if (threadIdx.x < a.rows) {
       const int row = threadIdx.x;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < TPS; ++w) M = fmaxf(M, stat_m[w * C::kRows + row]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float Ls = 0.f;
-#pragma unroll
-      for (int w = 0; w < TPS; ++w)
-        Ls += stat_l[w * C::kRows + row] * ex2(stat_m[w * C::kRows + row] - Mu);
-      const float lse = Ls > 0.f ? (Mu + log2f(Ls)) * kLn2 : -INFINITY;
+      const float lse = row_lse(row);
       const int t = row / a.group;
       const int h = kvh * a.group + (row - t * a.group);
       const int64_t prow = (static_cast<int64_t>(b) * a.q_len + t) * a.num_q_heads + h;
@@ -940,6 +1070,14 @@ cudaError_t launch_split(const CUtensorMap& k_map, const CUtensorMap& v_map, con
                          : launch_nt<1, false, false>(k_map, v_map, a, stream);
   return cluster_merge ? launch_nt<2, true, false>(k_map, v_map, a, stream)
                        : launch_nt<2, false, false>(k_map, v_map, a, stream);
+}
+
+int split_box_tokens(int rows, bool fp8, bool paged, int64_t ctas) {
+  if (paged || rows > kMaxNarrowRows) return kTileTokens;  // pages, or the tcgen05 kernel
+  if (fp8) return kTileTokens * (rows <= 8 ? Variant<1, false, true>::kTps
+                                           : Variant<2, false, true>::kTps);
+  return kTileTokens * (deep_grid(false, ctas) ? Variant<1, false, false, true>::kTps
+                                               : Variant<1, false, false>::kTps);
 }
 
 int split_ctas_per_sm(int rows, bool fp8) {

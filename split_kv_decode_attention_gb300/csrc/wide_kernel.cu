@@ -68,7 +68,6 @@ constexpr int kWTiles = kWTok / kTileTokens; // 16-token page tiles per stage
 #ifndef DATTN_WIDE_F8_OPS
 #define DATTN_WIDE_F8_OPS 3
 #endif
-constexpr int kWSoftmaxThreads = 256;
 constexpr int kWHalf = kWTok * 128;          // [64 tokens][64 d] 16-bit = 8 KB
 constexpr int kWStageBytes = 4 * kWHalf;     // operand stage: K halves, then V halves
 constexpr int kWF8Tile = kTileTokens * 128;  // one FP8 tile (K or V): 16 rows of 128 bytes
