@@ -561,9 +561,10 @@ def run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev):
     return {"value": round(nbytes["kv"] / med / 1e9, 2), "unit": "GB/s",
             "us_per_call": round(med * 1e6, 2), "h2d_bytes_per_step": int(bi),
             "d2h_bytes_per_step": int(bo), "steps": len(times),
-            "api": "decode_attn_host (C ABI): q, seq_lens, block table from pinned host memory, "
-                   "out and lse to pinned host memory, copies and stream sync inside the call; "
-                   "K/V cache resident"}
+            "api": "decode_attn_host (C ABI): q, seq_lens, block table in page-locked host "
+                   "memory, out and lse back to page-locked host memory; the kernels read and "
+                   "write them in place over the GPU's mapping of host memory (NVLink-C2C), "
+                   "stream sync inside the call; K/V cache resident"}
 
 
 # ---------------------------------------------------------------- reference arm

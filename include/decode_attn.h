@@ -239,17 +239,18 @@ int decode_attn_workspace_bytes(const decode_attn_params *p, int32_t num_splits,
  * decode_attn_plan()'s rule to the current seq_lens (the same plan the host
  * planner gives for those lengths), then the split kernel runs one CTA per
  * item slot of a capacity fixed by the shape (B x Hkv + 16 waves of resident
- * CTAs), then the combine: three launches, no host synchronisation, graph
- * capturable.  If the rule's chunk would make more (request, kv head, chunk)
- * items than the capacity, the chunk grows until they fit.  Workspace layout
- * (offsets rounded up to 256 bytes): int32 plan[4] = {chunk_len, items,
- * chunks of the longest request, capacity}; int32 pre[B + 1], the exclusive
- * prefix over requests of their chunk counts; int4 items[capacity] = (b, kv
- * head, chunk, clamped length) in (request, kv head, chunk) order; fp32
- * partial outputs [capacity, rows, D] and partial LSEs [capacity, rows], item
- * i = pre[b] * Hkv + kvh * n_b + s holding row r = t * G + g of that (b, kvh)
- * (n_b = max(1, ceil(L_b / chunk_len)) chunks).  One request keeps the host
- * plan (from max_seq_len) and, where it fits, the cluster merge.
+ * CTAs), then the combine kernel merges: three launches, no host
+ * synchronisation, graph capturable.  If the rule's chunk would make more
+ * (request, kv head, chunk) items than the capacity, the chunk grows until
+ * they fit.  Workspace layout (offsets rounded up to 256 bytes): int32
+ * plan[4] = {chunk_len, items, chunks of the longest request, capacity};
+ * int32 pre[B + 1], the exclusive prefix over requests of their chunk
+ * counts; int4 items[capacity] = (b, kv head, chunk, clamped length) in
+ * (request, kv head, chunk) order; fp32 partial outputs [capacity, rows, D]
+ * and partial LSEs [capacity, rows], item i = pre[b] * Hkv + kvh * n_b + s
+ * holding row r = t * G + g of that (b, kvh) (n_b = max(1, ceil(L_b /
+ * chunk_len)) chunks).  One request keeps the host plan (from max_seq_len)
+ * and, where it fits, the cluster merge.
  */
 int decode_attn(const decode_attn_params *p, const void *q, const void *k_cache,
                 const void *v_cache, const int32_t *block_table,
@@ -323,11 +324,16 @@ int decode_attn_static_workspace(const decode_attn_params *p, const void *q,
  * decode_attn() with the per-call inputs and outputs in host memory: the call
  * a serving loop makes when q, seq_lens and the block table arrive from the
  * host and out / lse go back to it, while the K/V cache stays resident on the
- * device.  One call copies q, seq_lens and the block table into device
- * staging buffers carved from `workspace`, runs the same kernels as
- * decode_attn(), copies out and lse (and the status word) back, and returns
- * once `stream` has finished the call's work.  Unlike every other entry it
- * synchronises the stream, so it cannot be captured in a CUDA graph.
+ * device.  It runs the same kernels as decode_attn() and returns once
+ * `stream` has finished the call's work.  When q, seq_lens, the block table,
+ * out and lse are all page-locked (cudaHostAlloc / cudaHostRegister), the
+ * kernels read and write them in place through the GPU's mapping of host
+ * memory (NVLink-C2C on Grace systems): no staging copies; a page-locked
+ * status word is zeroed and written in place too.  Otherwise the call copies
+ * q, seq_lens and the block table into device staging buffers carved from
+ * `workspace` and copies out and lse (and the status word) back.  Unlike every
+ * other entry it synchronises the stream, so it cannot be captured in a CUDA
+ * graph.
  *   q_host            bf16 [B, q_len, Hq, 128] in host memory, dense: the
  *                     params' q strides must be the packed ones
  *   k_cache, v_cache  the device caches, as for decode_attn()
@@ -346,8 +352,8 @@ int decode_attn_static_workspace(const decode_attn_params *p, const void *q,
  *                     partials of decode_attn(), then the staging buffers
  *   status_host       optional int32 host word: the call's DA_STATUS_* bits
  *   stream            cudaStream_t (NULL: legacy default stream)
- * Page-locked host buffers (cudaHostAlloc / cudaHostRegister) let the copies
- * run at full speed; pageable memory works through the driver's staging.
+ * Page-locked host buffers (cudaHostAlloc / cudaHostRegister) take the
+ * direct path above; pageable memory works through staging copies.
  * Argument errors return before anything is copied or launched; a failure
  * after the copies were queued waits for the stream, then returns the code.
  */

@@ -263,8 +263,9 @@ def decode_attn_host(q_host, k_cache, v_cache, block_table_host, seq_lens_host, 
                      two_pass: bool = False, k_scale: float = 1.0, v_scale: float = 1.0):
     """decode_attn with q, block table and seq_lens in host memory (torch CPU
     tensors, ideally pinned) and out / lse returned to host memory; the K/V
-    cache stays on the device.  One C call: copies in, kernels, copies out,
-    stream synchronised.  Returns (out_host, lse_host, status bits)."""
+    cache stays on the device.  One C call: with pinned buffers the kernels
+    read and write them in place, otherwise copies in and out; the stream is
+    synchronised.  Returns (out_host, lse_host, status bits)."""
     import numpy as np
     import torch
 
@@ -276,19 +277,25 @@ def decode_attn_host(q_host, k_cache, v_cache, block_table_host, seq_lens_host, 
     p = params if params is not None else params_from_tensors(
         q_host, k_cache, block_table_host, max_seq_len=max_seq_len, causal=causal, scale=scale,
         out=out_host, two_pass=two_pass, k_scale=k_scale, v_scale=v_scale)
-    if num_splits <= 0:  # the library's planner, with the actual lengths
-        num_splits, _ = decode_attn_plan(p, np.asarray(seq_lens_host, dtype=np.int32))
-    need = decode_attn_host_workspace_bytes(p, num_splits)
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
+    if workspace is None:   # (a given workspace is checked by the C call itself)
+        if num_splits <= 0:  # the library's planner, with the actual lengths
+            num_splits, _ = decode_attn_plan(p, np.asarray(seq_lens_host, dtype=np.int32))
+        need = decode_attn_host_workspace_bytes(p, num_splits)
         workspace = torch.empty((need + 15) // 16 * 4, dtype=torch.float32, device=k_cache.device)
-    status = ctypes.c_int32(0)
+    global _host_status
+    if _host_status is None:   # a page-locked word: the kernels write it in place
+        _host_status = torch.zeros(1, dtype=torch.int32).pin_memory()
+    status_ptr = _host_status.data_ptr()
     _check(lib().decode_attn_host(ctypes.byref(p), _ptr(q_host), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(block_table_host), _ptr(seq_lens_host), _ptr(out_host),
                                   _ptr(lse_host), int(num_splits), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(),
-                                  ctypes.byref(status), _stream_handle(stream)),
+                                  status_ptr, _stream_handle(stream)),
            "decode_attn_host")
-    return out_host, lse_host, status.value
+    return out_host, lse_host, ctypes.c_int32.from_address(status_ptr).value
+
+
+_host_status = None
 
 
 def decode_attn_device_plan(p: DecodeAttnParams, seq_lens, workspace, status=None, stream=None):

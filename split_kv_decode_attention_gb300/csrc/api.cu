@@ -160,6 +160,27 @@ int plan_impl(const decode_attn_params* p, const int32_t* host_seq_lens, int32_t
 
 // box_tokens: token rows per box (16; a whole stage for contiguous caches
 // on the warp-MMA kernel)
+// Encoded tensor maps of recent calls: a serving loop passes the same caches
+// every step, so the map of (base, layout, box) is encoded once and reused.
+struct MapKey {
+  const void* base;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box;
+  int fp8;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && std::memcmp(dims, o.dims, sizeof(dims)) == 0 &&
+           std::memcmp(strides, o.strides, sizeof(strides)) == 0 && box == o.box && fp8 == o.fp8;
+  }
+};
+constexpr int kMapCacheSize = 16;
+std::mutex g_map_mu;
+struct {
+  MapKey key;
+  CUtensorMap map;
+  bool valid;
+} g_map_cache[kMapCacheSize];
+int g_map_next = 0;
+
 int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p, bool paged,
                 int box_tokens) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -181,11 +202,33 @@ int make_kv_map(CUtensorMap* map, const void* base, const decode_attn_params* p,
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 1,
                              static_cast<cuuint32_t>(box_tokens), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.base = base;
+  std::memcpy(key.dims, dims, sizeof(dims));
+  std::memcpy(key.strides, strides, sizeof(strides));
+  key.box = box[2];
+  key.fp8 = kv_fp8(p) ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (auto& e : g_map_cache)
+      if (e.valid && e.key == key) {
+        *map = e.map;
+        return DA_OK;
+      }
+  }
   CUresult r = enc(map, kv_fp8(p) ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                    4, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DA_OK : DA_ERR_ALIGNMENT;
+  if (r != CUDA_SUCCESS) return DA_ERR_ALIGNMENT;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  auto& e = g_map_cache[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCacheSize;
+  e.key = key;
+  e.map = *map;
+  e.valid = true;
+  return DA_OK;
 }
 
 bool stride_ok(int64_t s) { return s > 0 && s % 8 == 0 && s * 2 < (1LL << 40); }
@@ -655,6 +698,20 @@ int host_layout(const decode_attn_params* p, int32_t num_splits, bool paged, Hos
   return DA_OK;
 }
 
+// The device's address of a page-locked host buffer (cudaHostAlloc /
+// cudaHostRegister; also what torch's pin_memory gives), or false for
+// pageable memory and anything else.
+bool device_view(const void* host, const void** dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    cudaGetLastError();  // (an unknown pointer is not an error here)
+    return false;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return false;
+  *dev = at.devicePointer;
+  return true;
+}
+
 // Element (b, t, h, d) at ((b * q_len + t) * Hq + h) * 128 + d (strides of
 // dimensions of extent 1 do not matter).
 bool dense_rows(int64_t sb, int64_t st, int64_t sh, const decode_attn_params* p) {
@@ -733,11 +790,42 @@ int decode_attn_host(const decode_attn_params* p, const void* q_host, const void
   const size_t rows = static_cast<size_t>(p->batch) * p->q_len * p->num_q_heads;
   const size_t bt_bytes = paged ? static_cast<size_t>(p->batch) * p->block_table_stride * 4 : 0;
   auto finish = [&](int code) {
-    // the queued copies read or write the caller's host buffers: they must
-    // be done before the call returns, whatever the outcome
+    // the queued work reads or writes the caller's host buffers: it must be
+    // done before the call returns, whatever the outcome
     if (cudaStreamSynchronize(st) != cudaSuccess && code == DA_OK) code = DA_ERR_CUDA;
     return code;
   };
+
+  // Page-locked buffers: the kernels read q, the lengths and the block table
+  // and write out and lse in host memory directly (over NVLink-C2C on Grace
+  // systems), so the call is the kernels and one synchronise -- no staging
+  // copies.  A page-locked status word is zeroed and written in place; any
+  // other one goes through a workspace word.
+  const void *q_d = nullptr, *lens_d = nullptr, *bt_d = nullptr, *out_d = nullptr,
+             *lse_d = nullptr, *st_d = nullptr;
+  if (device_view(q_host, &q_d) && device_view(seq_lens_host, &lens_d) &&
+      (!paged || device_view(block_table_host, &bt_d)) && device_view(out_host, &out_d) &&
+      device_view(lse_host, &lse_d)) {
+    int32_t* status_dev = nullptr;
+    if (status_host != nullptr) {
+      if (device_view(status_host, &st_d)) {
+        *status_host = 0;
+        status_dev = static_cast<int32_t*>(const_cast<void*>(st_d));
+      } else {
+        status_dev = reinterpret_cast<int32_t*>(w + h.status);
+        if (cudaMemsetAsync(status_dev, 0, 4, st) != cudaSuccess) return finish(DA_ERR_CUDA);
+      }
+    }
+    rc = run_decode(p, q_d, k_cache, v_cache, static_cast<const int32_t*>(bt_d),
+                    static_cast<const int32_t*>(lens_d), const_cast<void*>(out_d),
+                    static_cast<float*>(const_cast<void*>(lse_d)), num_splits, w + h.part, h.q,
+                    status_dev, stream, true);
+    if (rc != DA_OK) return finish(rc);
+    if (status_host != nullptr && st_d == nullptr &&
+        cudaMemcpyAsync(status_host, w + h.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return finish(DA_ERR_CUDA);
+    return finish(DA_OK);
+  }
   if (cudaMemcpyAsync(w + h.q, q_host, rows * kHeadDim * 2, cudaMemcpyHostToDevice, st) !=
           cudaSuccess ||
       cudaMemcpyAsync(w + h.lens, seq_lens_host, static_cast<size_t>(p->batch) * 4,

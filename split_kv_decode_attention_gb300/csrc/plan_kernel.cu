@@ -28,31 +28,41 @@
 namespace dattn {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
 constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kPlanLenCache = 4096;  // clamped lengths kept in shared memory
 
 struct PlanSmem {
-  long long red[kPlanWarps];
+  long long red[2][kPlanWarps];  // block sums, two buffers used alternately
+  long long scan[kPlanWarps];    // warp totals of the prefix
   int lens[kPlanLenCache];
 };
 
-// Sum of v over the block (every thread gets it).  All threads must call it.
-__device__ long long block_sum(long long v, PlanSmem& sm) {
+// Sum of v over the block (every thread gets it).  All threads call it; the
+// two buffers alternate, so one barrier per call suffices (a buffer is written
+// again only after every thread passed the barrier of the call in between).
+__device__ long long block_sum(long long v, PlanSmem& sm, int& parity) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();  // the previous call's readers are done with red[]
-  if (lane == 0) sm.red[warp] = v;
+  if (lane == 0) sm.red[parity][warp] = v;
   __syncthreads();
-  long long t = lane < kPlanWarps ? sm.red[lane] : 0;
+  long long t = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  for (int w = 0; w < kPlanWarps; ++w) t += sm.red[parity][w];
+  parity ^= 1;
   return t;
+}
+
+// ceil(L / c) for 0 < L < 2^31, 0 < c <= 2^30 (32-bit unsigned arithmetic)
+__device__ __forceinline__ int ceil_div_u(int L, long long c) {
+  const unsigned cu = static_cast<unsigned>(c);
+  return static_cast<int>((static_cast<unsigned>(L) + cu - 1u) / cu);
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs a) {
   __shared__ PlanSmem sm;
+  int parity = 0;
   // launched early behind the previous kernel, which may write seq_lens
   grid_dependency_wait();
   // the split kernel may start launching: it waits for this grid's writes
@@ -65,18 +75,20 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs a)
 
   // ---- lengths: clamp, report, sum, and whether they are all equal
   const int raw0 = a.seq_lens[0];
-  long long work = 0, diff = 0, bad = 0;
+  long long work = 0;
+  bool diff = false;
+  uint32_t bad = 0;
   for (int b = tid; b < B; b += kPlanThreads) {
     const int raw = a.seq_lens[b];
     const int L = clamp_len(raw);
     if (raw != L) bad |= DA_STATUS_SEQ_LEN;
     if (a.causal && L > 0 && L < a.q_len) bad |= DA_STATUS_SHORT_CAUSAL;
-    if (raw != raw0) diff = 1;
+    diff = diff || raw != raw0;
     if (b < kPlanLenCache) sm.lens[b] = L;
     work += L;
   }
-  work = block_sum(work, sm);
-  const bool uniform = __syncthreads_or(diff != 0) == 0;
+  work = block_sum(work, sm, parity);  // (its barrier also publishes sm.lens)
+  const bool uniform = __syncthreads_or(diff) == 0;
   uint32_t bits = 0;
   if (__syncthreads_or((bad & DA_STATUS_SEQ_LEN) != 0)) bits |= DA_STATUS_SEQ_LEN;
   if (__syncthreads_or((bad & DA_STATUS_SHORT_CAUSAL) != 0)) bits |= DA_STATUS_SHORT_CAUSAL;
@@ -84,12 +96,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs a)
 
   // work items at chunk length c (a block-wide sum; all threads call it)
   auto chunks_of = [&](long long c) -> long long {
+    // (every length is <= max_seq_len <= 2^30 here, so a longer chunk
+    // counts one per request, the same as 2^30)
+    const long long cc = c < (1LL << 30) ? c : (1LL << 30);
     long long n = 0;
     for (int b = tid; b < B; b += kPlanThreads) {
-      const long long L = len_of(b);
-      n += L > 0 ? (L + c - 1) / c : 1;
+      const int L = len_of(b);
+      n += L > 0 ? ceil_div_u(L, cc) : 1;
     }
-    return block_sum(n, sm) * a.num_kv_heads;
+    return block_sum(n, sm, parity) * a.num_kv_heads;
   };
 
   PlanShape shape;
@@ -123,23 +138,25 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanArgs a)
   long long run = 0;
   for (int b0 = 0; b0 < B; b0 += kPlanThreads) {
     const int b = b0 + tid;
-    const long long L = b < B ? len_of(b) : 0;
-    const long long n = b < B ? (L > 0 ? (L + chunk - 1) / chunk : 1) : 0;
+    const int L = b < B ? len_of(b) : 0;
+    const long long n = b < B ? (L > 0 ? ceil_div_u(L, chunk) : 1) : 0;
     long long x = n;  // inclusive warp scan
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const long long y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
+    if (lane == 31) sm.scan[warp] = x;
     __syncthreads();
-    if (lane == 31) sm.red[warp] = x;
-    __syncthreads();
-    long long before = 0;
-    for (int w = 0; w < warp; ++w) before += sm.red[w];
+    long long before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kPlanWarps; ++w) {
+      before += w < warp ? sm.scan[w] : 0;
+      tot += sm.scan[w];
+    }
     if (b < B) a.pre[b] = static_cast<int32_t>(run + before + x - n);
-    long long tot = 0;
-    for (int w = 0; w < kPlanWarps; ++w) tot += sm.red[w];
     run += tot;
+    __syncthreads();  // sm.scan is rewritten by the next round
   }
   if (tid == 0) a.pre[B] = static_cast<int32_t>(run);
   __syncthreads();  // pre[] visible to the whole block

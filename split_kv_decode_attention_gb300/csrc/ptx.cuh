@@ -133,6 +133,23 @@ __device__ __forceinline__ float4 ld_global_hint(const float* ptr, uint64_t pol)
   return v;
 }
 
+// As ld_global_hint, through L2 only (.cg): for data that other CTAs of the
+// same kernel wrote (the L1 of this SM may not see their writes).
+__device__ __forceinline__ float4 ld_global_cg_hint(const float* ptr, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(ptr), "l"(pol)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ld_global_cg_hint1(const float* ptr, uint64_t pol) {
+  float v;
+  asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(ptr), "l"(pol) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float ld_global_hint1(const float* ptr, uint64_t pol) {
   float v;
   asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(ptr), "l"(pol) : "memory");

@@ -142,7 +142,7 @@ def test_device_planned_call_matches_oracle_and_host_plan_bits(binding, case):
     q, k, v, bt, lens = to_device(inp)
     p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=causal,
                                     k_scale=inp.k_scale, v_scale=inp.v_scale)
-    assert binding.decode_attn_launch_count(p, 0) == 3
+    assert binding.decode_attn_launch_count(p, 0) == 3      # planner, split, combine
     out, lse, st = run_auto(binding, inp, num_splits=0)
     assert st == 0
     ref_o, ref_l = oracle.decode_attention_inputs(inp)
@@ -223,3 +223,40 @@ def test_captured_graph_replans_when_lengths_change(binding, wide):
         assert (int(plan[0].item()), int(plan[2].item())) == (chunk, S)
         plans.add(int(plan[0].item()))
     assert len(plans) >= 2          # the replays really planned differently
+
+
+@pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "fp8"])
+def test_device_plan_with_more_than_32_chunks_per_request(binding, fp8):
+    """A small ragged batch whose long request the planner cuts into > 32
+    chunks (the combine's multi-group path), called twice on one workspace:
+    identical bits both times and to the explicit two-pass call with the
+    host's plan, and the oracle's result."""
+    lens = np.array([30000, 100, 0, 4097, 16], np.int32)
+    shp = W.small_shape("many_chunks", batch=len(lens), q_len=2, num_q_heads=8, num_kv_heads=2,
+                        lo=1, hi=30000, causal=True, seed=18, kv_fp8=fp8)
+    inp = W.make_host_inputs(shp, seq_lens=np.maximum(lens, 2))
+    inp.seq_lens[2] = 0                               # an empty request
+    q, k, v, bt, lens_d = to_device(inp)
+    p = binding.params_from_tensors(q, k, bt, max_seq_len=inp.max_seq_len, causal=True,
+                                    k_scale=inp.k_scale, v_scale=inp.v_scale)
+    ws = torch.empty((binding.decode_attn_workspace_bytes(p, 0) + 3) // 4, dtype=torch.float32,
+                     device="cuda")
+    outs = []
+    for splits in (0, 0, binding.decode_attn_plan(p, inp.seq_lens)[0]):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, lse = binding.decode_attn(q, k, v, bt, lens_d, max_seq_len=inp.max_seq_len,
+                                       num_splits=splits, workspace=ws if splits == 0 else None,
+                                       status=status, causal=True, two_pass=splits > 0,
+                                       k_scale=inp.k_scale, v_scale=inp.v_scale)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append((bf16_tensor_to_bits(out), lse.cpu().numpy().view(np.uint32)))
+        if splits == 0:
+            plan, _, _ = binding.device_plan_view(ws, p)
+            assert int(plan[2].item()) > 32           # the long request's chunks
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+    ref_o, ref_l = oracle.decode_attention_inputs(inp)
+    out_f = torch.from_numpy(outs[0][0].view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert_out_close(out_f.astype(np.float64), ref_o)
+    assert_lse_close(outs[0][1].view(np.float32), ref_l)
