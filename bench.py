@@ -427,6 +427,25 @@ def measure(args, dist: "Dist", binding, name: str, dev, clocks: "ClockSampler",
         warm = {"us_per_call": round(warm_us, 2),
                 "GB_s": round(nbytes["kv"] / (warm_us * 1e-6) / 1e9, 2),
                 "note": "K/V warm in L2 (no flush between calls); informational, not the value"}
+        # the same call with every length 0: the same grid, clusters and
+        # launches with no K/V to stream -- the floor a call of this shape
+        # pays before any byte is read (informational)
+        zero = torch.zeros_like(lens)
+        fev = []
+        for _ in range(min(args.steps, 200)):
+            flush_buf.fill_(1)
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            binding.decode_attn_split(p, q, k, v, bt, zero, out, lse, S, workspace=ws,
+                                      status=status, stream=stream)
+            if launches > 1:
+                binding.decode_attn_combine(p, zero, S, chunk, ws, out, lse, stream=stream)
+            b_ev.record(stream)
+            fev.append((a_ev, b_ev))
+        torch.cuda.synchronize()
+        warm["launch_floor_us"] = round(float(np.median([a.elapsed_time(b) for a, b in fev])) * 1e3, 2)
+        warm["launch_floor_note"] = ("the same launches with every seq_len 0 (no K/V read), flushed; "
+                                     "the per-call floor of this shape")
 
     e2e = run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev)
     cpu = None
@@ -542,13 +561,21 @@ def run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev):
         (0 if bt_h is None else bt_h.numel() * 4)
     bo = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
 
+    # the C entry point called directly with prepared arguments, as a native
+    # serving loop calls it (the binding's own per-call Python work excluded)
+    import ctypes
+    status_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    c_args = (ctypes.byref(p), q_h.data_ptr(), inp.k_cache.data_ptr(), inp.v_cache.data_ptr(),
+              None if bt_h is None else bt_h.data_ptr(), lens_h.data_ptr(), out_h.data_ptr(),
+              lse_h.data_ptr(), int(S), ws_h.data_ptr(), ws_h.numel() * 4, status_h.data_ptr(),
+              stream.cuda_stream)
+    fn = binding.lib().decode_attn_host
+    st_word = ctypes.c_int32.from_address(status_h.data_ptr())
+
     def one():
-        _, _, st = binding.decode_attn_host(q_h, inp.k_cache, inp.v_cache, bt_h, lens_h,
-                                            max_seq_len=inp.max_seq_len, num_splits=S,
-                                            out_host=out_h, lse_host=lse_h, workspace=ws_h,
-                                            params=p, stream=stream)
-        if st != 0:
-            raise SystemExit(f"device status {st} in the end-to-end call")
+        rc = fn(*c_args)
+        if rc != 0 or st_word.value != 0:
+            raise SystemExit(f"end-to-end call: rc {rc}, device status {st_word.value}")
 
     for _ in range(5):
         one()
@@ -561,10 +588,11 @@ def run_e2e(args, binding, inp, p, S, ws, out, lse, stream, nbytes, dev):
     return {"value": round(nbytes["kv"] / med / 1e9, 2), "unit": "GB/s",
             "us_per_call": round(med * 1e6, 2), "h2d_bytes_per_step": int(bi),
             "d2h_bytes_per_step": int(bo), "steps": len(times),
-            "api": "decode_attn_host (C ABI): q, seq_lens, block table in page-locked host "
-                   "memory, out and lse back to page-locked host memory; the kernels read and "
-                   "write them in place over the GPU's mapping of host memory (NVLink-C2C), "
-                   "stream sync inside the call; K/V cache resident"}
+            "api": "decode_attn_host (C ABI, called through ctypes with prepared arguments): q, "
+                   "seq_lens, block table in page-locked host memory, out and lse back to "
+                   "page-locked host memory; the kernels read and write them in place over the "
+                   "GPU's mapping of host memory (NVLink-C2C), stream sync inside the call; K/V "
+                   "cache resident"}
 
 
 # ---------------------------------------------------------------- reference arm

@@ -868,6 +868,13 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
 #endif
 constexpr int kStages = DATTN_STAGES;
 constexpr int kTilesPerStage = DATTN_TILES_PER_STAGE;
+// the 16-row bf16 variant (overridable for sweeps)
+#ifndef DATTN_NT2_STAGES
+#define DATTN_NT2_STAGES DATTN_STAGES
+#endif
+#ifndef DATTN_NT2_TILES_PER_STAGE
+#define DATTN_NT2_TILES_PER_STAGE DATTN_TILES_PER_STAGE
+#endif
 // FP8 caches: tiles are half the bytes; 4 stages (32 KB) leave room for 5-6
 // CTAs per SM, which the latency-bound 16-row FP8 variant needs (GB300: 4
 // stages 150 us, 6 stages 156 us on 32 requests x q_len 4; B = 1 unchanged)
@@ -895,9 +902,11 @@ constexpr int kDeepTilesPerStage = 4;
 template <int NT, bool CM, bool F8, bool DP = false>
 struct Variant {
   static_assert(!(F8 && DP), "the deep shape serves bf16 caches");
-  static constexpr int kSt = F8 ? kF8Stages : DP ? kDeepStages : kStages;
+  static constexpr int kSt = F8 ? kF8Stages : DP ? kDeepStages
+                                           : NT == 2 ? DATTN_NT2_STAGES : kStages;
   static constexpr int kTps = F8 ? (NT == 2 ? DATTN_F8_NT2_TILES_PER_STAGE : kF8TilesPerStage)
-                              : DP ? kDeepTilesPerStage : kTilesPerStage;
+                              : DP ? kDeepTilesPerStage
+                                   : NT == 2 ? DATTN_NT2_TILES_PER_STAGE : kTilesPerStage;
   using C = SplitCfg<NT, kSt, kTps, F8>;
   static constexpr auto kernel = split_kv_kernel<NT, kSt, kTps, CM, F8>;
 };
