@@ -119,10 +119,11 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock, LISTED ? kBlocksPerSm - 1
   // chunk length first (one more round trip).
   constexpr int kBatch = 4;
   const uint64_t dead = l2_evict_first_policy();  // each partial is read once
-  const float* pl;
-  const float* po;
-  int ls, os;  // per-split strides (<= 128 rows x 128 d)
-  int S, L, n;
+  // (set by the grid-planned path; the listed one returns before their use)
+  const float* pl = nullptr;
+  const float* po = nullptr;
+  int ls = 0, os = 0;  // per-split strides (<= 128 rows x 128 d)
+  int S = 0, L = 0, n = 0;
   if constexpr (LISTED) {
     L = a.seq_lens[b];
     const int pb = a.pre[b];

@@ -270,6 +270,13 @@ __device__ __forceinline__ float packed_pair_sum(uint32_t v, bool f16) {
   return packed_lo(v, f16) + packed_hi(v, f16);
 }
 
+// max(a, b, c) in one instruction (sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // bf16x2 -> f16x2; exact for magnitudes in f16's normal range [2^-14, 65504].
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));

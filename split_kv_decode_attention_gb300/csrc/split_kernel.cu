@@ -120,15 +120,22 @@ __device__ __forceinline__ uint32_t load_u32(const uint16_t* p) {
 // thread-block cluster; instead of writing fp32 partials for the combine
 // kernel they merge their results through distributed shared memory and write
 // the final output themselves.
-template <int NT, int STAGES, int TPS, bool CM, bool F8>
+// LS (listed): a device-planned call; CTA i takes item slot i of the device
+// planner's list.  A separate instantiation, because a CTA's (chunk, kv head,
+// request) read from memory is per-thread data to the compiler, while the
+// grid-planned variants take them from blockIdx and the kernel parameters as
+// warp-uniform values, so every index and address derived from them stays in
+// the uniform datapath instead of costing a per-thread instruction each.
+template <int NT, int STAGES, int TPS, bool CM, bool F8, bool LS>
 __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
     split_kv_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const SplitArgs a) {
+  static_assert(!(CM && LS), "a device-planned call writes partials");
   using C = SplitCfg<NT, STAGES, TPS, F8>;
   constexpr uint32_t kFull = 0xffffffffu;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool listed = !CM && a.items != nullptr;  // device-planned call
+  constexpr bool listed = LS;
 
   // launched early behind the previous kernel of the stream (or the device
   // planner): nothing it may write (q, caches, lengths, the plan, outputs)
@@ -137,7 +144,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
 
   // ---- this CTA's work item and key range [t_begin, t_end)
   int split, kvh, b, L, chunk;
-  if (listed) {
+  if constexpr (listed) {
     // item slot blockIdx.x of the planner's list (slots past its count exit)
     const int n_items = a.plan[1];
     const int4 itm = a.items[blockIdx.x];
@@ -156,7 +163,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
   }
   // the request length, clamped, with its status bits (grid-planned calls)
   auto take_length = [&]() {
-    if (listed) return;
+    if constexpr (listed) return;
     uint32_t bad = 0;
     if (L < 0 || L > a.max_seq_len) {
       bad |= DA_STATUS_SEQ_LEN;
@@ -512,7 +519,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
           const float p0 = ex2(x0 - m_use);
           const float p1 = ex2(x1 - m_use);
           l[nt][rr] = l[nt][rr] * alpha + (p0 + p1);
-          lq[nt][rr] *= alpha;
+          if constexpr (!F8) lq[nt][rr] *= alpha;
           m[nt][rr] = m_new;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
@@ -531,8 +538,12 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
         // key j0 (rows rr = 0 low, 1 high), then key j1
         const uint32_t k0 = F8 ? pack_f16x2(p[nt][0], p[nt][1]) : pack_bf16x2(p[nt][0], p[nt][1]);
         const uint32_t k1 = F8 ? pack_f16x2(p[nt][2], p[nt][3]) : pack_bf16x2(p[nt][2], p[nt][3]);
-        lq[nt][0] += packed_lo(k0, F8) + packed_lo(k1, F8);
-        lq[nt][1] += packed_hi(k0, F8) + packed_hi(k1, F8);
+        // bf16 P: the sums of the rounded weights normalise O (the FP8 path's
+        // f16 P rounds to 2^-11, well inside the bar: its fp32 sums serve)
+        if constexpr (!F8) {
+          lq[nt][0] += packed_lo(k0, false) + packed_lo(k1, false);
+          lq[nt][1] += packed_hi(k0, false) + packed_hi(k1, false);
+        }
         pb[nt][0] = movmatrix_trans(k0);
         pb[nt][1] = movmatrix_trans(k1);
       }
@@ -612,11 +623,15 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
       v += __shfl_xor_sync(kFull, v, 8);
       v += __shfl_xor_sync(kFull, v, 16);
       l[nt][rr] = v;
-      float w = lq[nt][rr];
-      w += __shfl_xor_sync(kFull, w, 4);
-      w += __shfl_xor_sync(kFull, w, 8);
-      w += __shfl_xor_sync(kFull, w, 16);
-      lq[nt][rr] = w;
+      if constexpr (F8) {
+        lq[nt][rr] = v;
+      } else {
+        float w = lq[nt][rr];
+        w += __shfl_xor_sync(kFull, w, 4);
+        w += __shfl_xor_sync(kFull, w, 8);
+        w += __shfl_xor_sync(kFull, w, 16);
+        lq[nt][rr] = w;
+      }
     }
   if (g4 == 0) {
 #pragma unroll
@@ -899,7 +914,7 @@ constexpr int kF8TilesPerStage = DATTN_F8_TILES_PER_STAGE;
 constexpr int kDeepStages = 3;
 constexpr int kDeepTilesPerStage = 4;
 
-template <int NT, bool CM, bool F8, bool DP = false>
+template <int NT, bool CM, bool F8, bool DP = false, bool LS = false>
 struct Variant {
   static_assert(!(F8 && DP), "the deep shape serves bf16 caches");
   static constexpr int kSt = F8 ? kF8Stages : DP ? kDeepStages
@@ -908,19 +923,19 @@ struct Variant {
                               : DP ? kDeepTilesPerStage
                                    : NT == 2 ? DATTN_NT2_TILES_PER_STAGE : kTilesPerStage;
   using C = SplitCfg<NT, kSt, kTps, F8>;
-  static constexpr auto kernel = split_kv_kernel<NT, kSt, kTps, CM, F8>;
+  static constexpr auto kernel = split_kv_kernel<NT, kSt, kTps, CM, F8, LS>;
 };
 
 constexpr int kMaxDev = 64;
 constexpr int kMaxCluster = 16;  // non-portable cluster size limit
 std::mutex g_attr_mu;
-bool g_attr_done[2][2][2][2][kMaxDev];
+bool g_attr_done[2][2][2][2][2][kMaxDev];
 // cached cudaOccupancyMaxActiveClusters per (NT, FP8, deep, cluster size, device); -1 unknown
 int g_max_clusters[2][2][2][kMaxCluster + 1][kMaxDev];
 bool g_max_clusters_init = false;
 int g_sm_count[kMaxDev];
 
-template <int NT, bool CM, bool F8, bool DP = false>
+template <int NT, bool CM, bool F8, bool DP = false, bool LS = false>
 cudaError_t ensure_attrs(int* dev_out = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -928,13 +943,13 @@ cudaError_t ensure_attrs(int* dev_out = nullptr) {
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   if (dev_out) *dev_out = dev;
   std::lock_guard<std::mutex> lk(g_attr_mu);
-  if (!g_attr_done[NT - 1][CM][F8][DP][dev]) {
-    e = cudaFuncSetAttribute(Variant<NT, CM, F8, DP>::kernel,
+  if (!g_attr_done[NT - 1][CM][F8][DP][LS][dev]) {
+    e = cudaFuncSetAttribute(Variant<NT, CM, F8, DP, LS>::kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Variant<NT, CM, F8, DP>::C::kSmemBytes);
+                             Variant<NT, CM, F8, DP, LS>::C::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (CM) {
-      e = cudaFuncSetAttribute(Variant<NT, CM, F8, DP>::kernel,
+      e = cudaFuncSetAttribute(Variant<NT, CM, F8, DP, LS>::kernel,
                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
     }
@@ -942,7 +957,7 @@ cudaError_t ensure_attrs(int* dev_out = nullptr) {
       e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
     }
-    g_attr_done[NT - 1][CM][F8][DP][dev] = true;
+    g_attr_done[NT - 1][CM][F8][DP][LS][dev] = true;
   }
   return cudaSuccess;
 }
@@ -957,14 +972,14 @@ bool deep_grid(bool fp8, int64_t ctas) {
   return ctas <= g_sm_count[dev];
 }
 
-template <int NT, bool CM, bool F8, bool DP>
+template <int NT, bool CM, bool F8, bool DP, bool LS>
 void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const SplitArgs& a,
                  cudaStream_t st) {
   cfg = {};
-  cfg.gridDim = a.items != nullptr ? dim3(static_cast<unsigned>(a.item_slots))
-                                   : dim3(a.num_splits, a.num_kv_heads, a.batch);
-  cfg.blockDim = dim3(Variant<NT, CM, F8, DP>::C::kThreads);
-  cfg.dynamicSmemBytes = Variant<NT, CM, F8, DP>::C::kSmemBytes;
+  cfg.gridDim = LS ? dim3(static_cast<unsigned>(a.item_slots))
+                   : dim3(a.num_splits, a.num_kv_heads, a.batch);
+  cfg.blockDim = dim3(Variant<NT, CM, F8, DP, LS>::C::kThreads);
+  cfg.dynamicSmemBytes = Variant<NT, CM, F8, DP, LS>::C::kSmemBytes;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -979,15 +994,24 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], const 
   }
 }
 
-template <int NT, bool CM, bool F8, bool DP = false>
-cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitArgs& a,
-                      cudaStream_t st) {
-  cudaError_t e = ensure_attrs<NT, CM, F8, DP>();
+template <int NT, bool CM, bool F8, bool DP, bool LS>
+cudaError_t launch_variant(const CUtensorMap& km, const CUtensorMap& vm, const SplitArgs& a,
+                           cudaStream_t st) {
+  cudaError_t e = ensure_attrs<NT, CM, F8, DP, LS>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  fill_config<NT, CM, F8, DP>(cfg, attr, a, st);
-  return cudaLaunchKernelEx(&cfg, Variant<NT, CM, F8, DP>::kernel, km, vm, a);
+  fill_config<NT, CM, F8, DP, LS>(cfg, attr, a, st);
+  return cudaLaunchKernelEx(&cfg, Variant<NT, CM, F8, DP, LS>::kernel, km, vm, a);
+}
+
+// the cluster-merge, listed (device-planned) or grid-planned variant
+template <int NT, bool CM, bool F8, bool DP = false>
+cudaError_t launch_nt(const CUtensorMap& km, const CUtensorMap& vm, const SplitArgs& a,
+                      cudaStream_t st) {
+  if constexpr (CM) return launch_variant<NT, true, F8, DP, false>(km, vm, a, st);
+  else if (a.items != nullptr) return launch_variant<NT, false, F8, DP, true>(km, vm, a, st);
+  else return launch_variant<NT, false, F8, DP, false>(km, vm, a, st);
 }
 
 // Resident CTAs per SM of a variant (queried once per device, then cached).

@@ -778,37 +778,59 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
 
       // ---- scale, masks (only on tiles that reach past this row's limit) and
       // the lazy running max
+      // With a positive scale the max of the scaled scores is the scale times
+      // the max of the raw ones, so the scores stay raw and the scale goes into
+      // the exponent's multiply-add below (s_fma; one multiply less per score);
+      // any other scale scales them here (s_fma = 1).
       const int tok0 = it.t_begin + j * kWTok;
+      const bool raw = a.scale_log2 > 0.f;
+      const float s_fma = raw ? a.scale_log2 : 1.f;
       float mt = -INFINITY;
-      if (tok0 + kWTok <= lim) {
+      if (raw) {
+        if (tok0 + kWTok <= lim) {
 #pragma unroll
-        for (int i = 0; i < kWTok; ++i) {
-          x[i] *= a.scale_log2;
-          mt = fmaxf(mt, x[i]);
+          for (int i = 0; i < kWTok; i += 2) mt = fmax3(mt, x[i], x[i + 1]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kWTok; i += 2) {
+            x[i] = tok0 + i < lim ? x[i] : -INFINITY;
+            x[i + 1] = tok0 + i + 1 < lim ? x[i + 1] : -INFINITY;
+            mt = fmax3(mt, x[i], x[i + 1]);
+          }
         }
+        mt *= a.scale_log2;
       } else {
 #pragma unroll
-        for (int i = 0; i < kWTok; ++i) {
+        for (int i = 0; i < kWTok; i += 2) {
           x[i] = tok0 + i < lim ? x[i] * a.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[i]);
+          x[i + 1] = tok0 + i + 1 < lim ? x[i + 1] * a.scale_log2 : -INFINITY;
+          mt = fmax3(mt, x[i], x[i + 1]);
         }
       }
       const bool raise = mt != -INFINITY && (m_used == -INFINITY || mt > m_used + kRescaleLog2);
       const float alpha = raise ? (m_used == -INFINITY ? 0.f : ex2(m_used - mt)) : 1.f;
       if (raise) m_used = mt;
       const float mref = m_used == -INFINITY ? 0.f : m_used;  // all masked so far: p = 0
+      // (pairs of scores in the packed two-wide fp32 instructions: half the
+      // issue slots for the exponent arguments and the running sums)
       uint32_t pk[kWTok / 2];
-      float psum = 0.f, qsum = 0.f;
+      float2 ps = make_float2(0.f, 0.f), qs = make_float2(0.f, 0.f);
+      const float2 s2 = make_float2(s_fma, s_fma);
+      const float2 nm2 = make_float2(-mref, -mref);
 #pragma unroll
       for (int i = 0; i < kWTok; i += 2) {
-        const float p0 = ex2(x[i] - mref);
-        const float p1 = ex2(x[i + 1] - mref);
-        psum += p0 + p1;
+        const float2 e = __ffma2_rn(make_float2(x[i], x[i + 1]), s2, nm2);
+        const float p0 = ex2(e.x);
+        const float p1 = ex2(e.y);
+        ps = __fadd2_rn(ps, make_float2(p0, p1));
         pk[i / 2] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-        qsum += packed_pair_sum(pk[i / 2], F8);
+        // bf16 P: the sum of the rounded weights normalises O (f16 P of the
+        // FP8 path rounds to 2^-11, well inside the bar: its fp32 sum serves)
+        if constexpr (!F8)
+          qs = __fadd2_rn(qs, make_float2(packed_lo(pk[i / 2], false), packed_hi(pk[i / 2], false)));
       }
-      l = l * alpha + psum;
-      lq = lq * alpha + qsum;
+      l = l * alpha + (ps.x + ps.y);
+      lq = F8 ? l : lq * alpha + (qs.x + qs.y);
 
       // ---- this group's previous P.V (tile j - 2) must be done before its O
       // is rescaled and its P buffer rewritten (the previous use may belong to
@@ -823,8 +845,13 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
             float o[32];
             tmem_ld32(lane_base + o_col + c * 32, o);
             tmem_wait_ld();
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = __fmul2_rn(make_float2(o[i], o[i + 1]), a2);
+              o[i] = v.x;
+              o[i + 1] = v.y;
+            }
             tmem_st32(lane_base + o_col + c * 32, o);
           }
           tmem_wait_st();
