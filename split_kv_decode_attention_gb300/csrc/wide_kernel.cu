@@ -940,34 +940,33 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     // (O is read out here, before this thread's next arrival on item_go lets
     // the next item's P.V overwrite it)
     // both buffers are read unconditionally (a buffer this item did not
-    // write holds stale values that the selects below drop), 16 columns at a
-    // time to keep the loop's live registers low
+    // write holds stale values that the selects below drop), 32 columns at a
+    // time (two TMEM round trips; the tile loop's registers are free by now)
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      const int d0 = grp * 64 + c * 16;
-      float o0[16], o1[16];
-      tmem_ld16(lane_base + kWColO + d0, o0);
-      tmem_ld16(lane_base + kWColO + kHeadDim + d0, o1);
+    for (int c = 0; c < 2; ++c) {
+      const int d0 = grp * 64 + c * 32;
+      float o0[32], o1[32];
+      tmem_ld32(lane_base + kWColO + d0, o0);
+      tmem_ld32(lane_base + kWColO + kHeadDim + d0, o1);
       tmem_wait_ld();
       if (r < a.rows) {
-        float o[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          o[i] = ((have0 ? o0[i] * f0 : 0.f) + (have1 ? o1[i] * f1 : 0.f)) * inv;
+        for (int i = 0; i < 32; ++i)
+          o0[i] = ((have0 ? o0[i] * f0 : 0.f) + (have1 ? o1[i] * f1 : 0.f)) * inv;
         if (direct) {
           uint16_t* dst = a.out + static_cast<int64_t>(it.b) * a.o_sb +
                           static_cast<int64_t>(t) * a.o_st + static_cast<int64_t>(h) * a.o_sh + d0;
 #pragma unroll
-          for (int i = 0; i < 16; i += 8)
+          for (int i = 0; i < 32; i += 8)
             *reinterpret_cast<uint4*>(dst + i) =
-                make_uint4(pack_bf16x2(o[i], o[i + 1]), pack_bf16x2(o[i + 2], o[i + 3]),
-                           pack_bf16x2(o[i + 4], o[i + 5]), pack_bf16x2(o[i + 6], o[i + 7]));
+                make_uint4(pack_bf16x2(o0[i], o0[i + 1]), pack_bf16x2(o0[i + 2], o0[i + 3]),
+                           pack_bf16x2(o0[i + 4], o0[i + 5]), pack_bf16x2(o0[i + 6], o0[i + 7]));
         } else {
           float* dst = a.part_o + pidx * kHeadDim + d0;
           const uint64_t keep = l2_evict_last_policy();
 #pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            st_global_hint(dst + i, make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]), keep);
+          for (int i = 0; i < 32; i += 4)
+            st_global_hint(dst + i, make_float4(o0[i], o0[i + 1], o0[i + 2], o0[i + 3]), keep);
         }
       }
     }
