@@ -327,9 +327,12 @@ int decode_attn_static_workspace(const decode_attn_params *p, const void *q,
  * device.  It runs the same kernels as decode_attn() and returns once
  * `stream` has finished the call's work.  When q, seq_lens, the block table,
  * out and lse are all page-locked (cudaHostAlloc / cudaHostRegister), the
- * kernels read and write them in place through the GPU's mapping of host
- * memory (NVLink-C2C on Grace systems): no staging copies; a page-locked
- * status word is zeroed and written in place too.  Otherwise the call copies
+ * kernels read seq_lens and write out and lse in place through the GPU's
+ * mapping of host memory (NVLink-C2C on Grace systems), and read q in place
+ * too when there are at most 16 query rows per KV head; the block table (and
+ * q above 16 rows) is first copied into `workspace` with one copy each,
+ * because the kernels read them many times or late.  A page-locked status
+ * word is zeroed and written in place too.  Otherwise the call copies
  * q, seq_lens and the block table into device staging buffers carved from
  * `workspace` and copies out and lse (and the status word) back.  Unlike every
  * other entry it synchronises the stream, so it cannot be captured in a CUDA

@@ -796,11 +796,16 @@ int decode_attn_host(const decode_attn_params* p, const void* q_host, const void
     return code;
   };
 
-  // Page-locked buffers: the kernels read q, the lengths and the block table
-  // and write out and lse in host memory directly (over NVLink-C2C on Grace
-  // systems), so the call is the kernels and one synchronise -- no staging
-  // copies.  A page-locked status word is zeroed and written in place; any
-  // other one goes through a workspace word.
+  // Page-locked buffers: the kernels read q and the lengths and write out and
+  // lse in host memory directly (over NVLink-C2C on Grace systems).  Two
+  // inputs are read too often or too late for that: the block table, whose
+  // entries the producers fetch one stage ahead of each copy, and q for the
+  // tcgen05 kernel, which stages each work item's rows while the previous one
+  // runs -- both go to the workspace first with one copy each (GB300, end to
+  // end: w64 278 -> 259 us, w128 192 -> 162 us; the warp-MMA kernel reads
+  // each query row once per CTA and keeps q in place).  A page-locked status
+  // word is zeroed and written in place; any other one goes through a
+  // workspace word.
   const void *q_d = nullptr, *lens_d = nullptr, *bt_d = nullptr, *out_d = nullptr,
              *lse_d = nullptr, *st_d = nullptr;
   if (device_view(q_host, &q_d) && device_view(seq_lens_host, &lens_d) &&
@@ -816,10 +821,23 @@ int decode_attn_host(const decode_attn_params* p, const void* q_host, const void
         if (cudaMemsetAsync(status_dev, 0, 4, st) != cudaSuccess) return finish(DA_ERR_CUDA);
       }
     }
-    rc = run_decode(p, q_d, k_cache, v_cache, static_cast<const int32_t*>(bt_d),
-                    static_cast<const int32_t*>(lens_d), const_cast<void*>(out_d),
-                    static_cast<float*>(const_cast<void*>(lse_d)), num_splits, w + h.part, h.q,
-                    status_dev, stream, true);
+    const int32_t* bt_use = static_cast<const int32_t*>(bt_d);
+    if (paged) {
+      if (cudaMemcpyAsync(w + h.bt, block_table_host, bt_bytes, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+        return finish(DA_ERR_CUDA);
+      bt_use = reinterpret_cast<const int32_t*>(w + h.bt);
+    }
+    const void* q_use = q_d;
+    if (rows_of(p) > dattn::kMaxNarrowRows) {
+      if (cudaMemcpyAsync(w + h.q, q_host, rows * kHeadDim * 2, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+        return finish(DA_ERR_CUDA);
+      q_use = w + h.q;
+    }
+    rc = run_decode(p, q_use, k_cache, v_cache, bt_use, static_cast<const int32_t*>(lens_d),
+                    const_cast<void*>(out_d), static_cast<float*>(const_cast<void*>(lse_d)),
+                    num_splits, w + h.part, h.q, status_dev, stream, true);
     if (rc != DA_OK) return finish(rc);
     if (status_host != nullptr && st_d == nullptr &&
         cudaMemcpyAsync(status_host, w + h.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
