@@ -65,8 +65,13 @@ constexpr int kWTiles = kWTok / kTileTokens; // 16-token page tiles per stage
 #ifndef DATTN_WIDE_F8_CONVERTERS
 #define DATTN_WIDE_F8_CONVERTERS 5
 #endif
-#ifndef DATTN_WIDE_F8_OPS
-#define DATTN_WIDE_F8_OPS 3
+// FP8: widened K and V live in separate rings (a K slot is free once S =
+// Q.K^T is done, a V slot only after P.V), 16 KB per slot
+#ifndef DATTN_WIDE_F8_OPK
+#define DATTN_WIDE_F8_OPK 2
+#endif
+#ifndef DATTN_WIDE_F8_OPV
+#define DATTN_WIDE_F8_OPV 4
 #endif
 constexpr int kWHalf = kWTok * 128;          // [64 tokens][64 d] 16-bit = 8 KB
 constexpr int kWStageBytes = 4 * kWHalf;     // operand stage: K halves, then V halves
@@ -87,8 +92,11 @@ static_assert(kWStatFloats * 4 <= kWStatBytes, "statistics buffer");
 //     holds the MMA operands directly (5 stages of 32 KB).
 //   FP8 caches: warps 0-7 softmax, 8..9 TMA producers, 10..14 converters,
 //     15 MMA; the TMA ring holds FP8 stages (4 x 16 KB: 8 boxes of 2 KB per 64
-//     keys), the converters widen each to an f16 operand stage in a 3-slot
-//     ring (the B operands of kind::f16 must be 16-bit).
+//     keys), the converters widen each stage's K into a ring of 2 f16 K slots
+//     and its V into a ring of 4 f16 V slots (16 KB each; the B operands of
+//     kind::f16 must be 16-bit).  A K slot is released as soon as its S =
+//     Q.K^T completes, a V slot only after its P.V, so the two rings hold
+//     each half only as long as it is needed.
 // Shared memory: TMA ring, operand ring (FP8 only), Q staging ([128 rows][16
 // chunks of 16 B], chunk c of row r at c ^ (r & 15)), the groups' merge
 // statistics (two buffers), schedule tables, barriers.
@@ -106,17 +114,23 @@ struct WCfg {
   static constexpr int kStages = F8 ? DATTN_WIDE_F8_STAGES : DATTN_WIDE_STAGES;  // TMA ring
   static constexpr int kLoadBytes = F8 ? 2 * kWTiles * kWF8Tile : kWStageBytes;
   static constexpr int kBoxes = F8 ? 2 * kWTiles : 4 * kWTiles;  // 2 KB boxes per stage
-  static constexpr int kOpStages = F8 ? DATTN_WIDE_F8_OPS : kStages;  // stages the MMA reads
+  // where the MMAs read K and V: the TMA ring itself (bf16: the two halves of
+  // each 32 KB stage), or the FP8 variant's widened K and V rings
+  static constexpr int kOpK = F8 ? DATTN_WIDE_F8_OPK : kStages;
+  static constexpr int kOpV = F8 ? DATTN_WIDE_F8_OPV : kStages;
+  static constexpr int kKSlotBytes = F8 ? 2 * kWHalf : kWStageBytes;  // K slot stride
+  static constexpr int kVSlotBytes = F8 ? 2 * kWHalf : kWStageBytes;  // V slot stride
   static constexpr int kOffLoad = 0;
-  static constexpr int kOffOp = F8 ? kOffLoad + kStages * kLoadBytes : kOffLoad;
-  static constexpr int kOffQ = F8 ? kOffOp + kOpStages * kWStageBytes : kOffLoad + kStages * kLoadBytes;
+  static constexpr int kOffOpK = F8 ? kOffLoad + kStages * kLoadBytes : kOffLoad;
+  static constexpr int kOffOpV = F8 ? kOffOpK + kOpK * kKSlotBytes : kOffLoad + 2 * kWHalf;
+  static constexpr int kOffQ = F8 ? kOffOpV + kOpV * kVSlotBytes : kOffLoad + kStages * kLoadBytes;
   static constexpr int kOffStat = kOffQ + kWRows * 256;
   static constexpr int kOffSched = kOffStat + 2 * kWStatBytes;
   static constexpr int kOffBar = kOffSched + ((kWSchedInts * 4 + 15) & ~15);
-  // full[], empty[] of the TMA ring, conv_full[], conv_empty[] of the operand
-  // ring (FP8), then s_full, s_free, p_full, pv_done per group, q_full,
-  // q_empty, item_go, grp_sync, tmem_done
-  static constexpr int kNumBars = 2 * kStages + (F8 ? 2 * kOpStages : 0) + 8 + 5;
+  // full[], empty[] of the TMA ring, then (FP8) full[] and empty[] of the K
+  // ring and of the V ring, then s_full, s_free, p_full, pv_done per group,
+  // q_full, q_empty, item_go, grp_sync, tmem_done
+  static constexpr int kNumBars = 2 * kStages + (F8 ? 2 * (kOpK + kOpV) : 0) + 8 + 5;
   static constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
   static_assert(kProducers >= 1 && kBoxes <= 32 * kProducers, "one box per producer lane");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -264,9 +278,11 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full_bar = bars;                   // [kStages] TMA bytes landed
   uint64_t* empty_bar = bars + C::kStages;     // [kStages] TMA slot free again
-  uint64_t* conv_full = empty_bar + C::kStages;                     // FP8: operand stage widened
-  uint64_t* conv_empty = conv_full + (F8 ? C::kOpStages : 0);       // FP8: operand stage consumed
-  uint64_t* s_full = conv_empty + (F8 ? C::kOpStages : 0);          // [2] scores in TMEM buffer
+  uint64_t* convk_full = empty_bar + C::kStages;                    // FP8: K slot widened
+  uint64_t* convk_empty = convk_full + (F8 ? C::kOpK : 0);          // FP8: K slot read by S
+  uint64_t* convv_full = convk_empty + (F8 ? C::kOpK : 0);          // FP8: V slot widened
+  uint64_t* convv_empty = convv_full + (F8 ? C::kOpV : 0);          // FP8: V slot read by P.V
+  uint64_t* s_full = convv_empty + (F8 ? C::kOpV : 0);              // [2] scores in TMEM buffer
   uint64_t* s_free = s_full + 2;               // [2] score buffer read by softmax
   uint64_t* p_full = s_free + 2;               // [2] P buffer (and O rescale) ready for PV
   uint64_t* pv_done = p_full + 2;              // [2] PV of that P buffer finished
@@ -289,9 +305,13 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       mbar_init(&empty_bar[s], F8 ? C::kConverters : 1);
     }
     if (F8) {
-      for (int o = 0; o < C::kOpStages; ++o) {
-        mbar_init(&conv_full[o], C::kConverters);
-        mbar_init(&conv_empty[o], 1);
+      for (int o = 0; o < C::kOpK; ++o) {
+        mbar_init(&convk_full[o], C::kConverters);
+        mbar_init(&convk_empty[o], 1);
+      }
+      for (int o = 0; o < C::kOpV; ++o) {
+        mbar_init(&convv_full[o], C::kConverters);
+        mbar_init(&convv_empty[o], 1);
       }
     }
     for (int i = 0; i < 2; ++i) {
@@ -517,65 +537,80 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
   }
 
   // ======================================================= FP8 converters
-  // Widen each landed FP8 stage to an f16 operand stage ([2 d-halves][64
-  // tokens][64 d], 128-byte swizzle): 16-byte chunk c of FP8 row t (d = 16c ..
+  // Widen each landed FP8 stage: its K tiles into the next K slot, then its V
+  // tiles into the next V slot, each an f16 operand ([2 d-halves][64 tokens]
+  // [64 d], 128-byte swizzle): 16-byte chunk c of FP8 row t (d = 16c ..
   // 16c+15) becomes 8-d chunks 2c and 2c+1 of d-half c / 4.  Each 8-lane
   // phase takes one chunk index of 8 consecutive rows, so loads (slot c ^ j)
-  // and stores ((2c & 7) ^ j, and ^ 1) hit 8 distinct bank groups.
+  // and stores ((2c & 7) ^ j, and ^ 1) hit 8 distinct bank groups.  V rows
+  // of keys past the item's chunk are written as zeros (their bytes may
+  // hold anything, and NaN * 0 is NaN in P.V).
   if (F8 && warp >= C::kConverterWarp && warp < C::kMmaWarp) {
     const int ct = tid - 32 * C::kConverterWarp;
     int gs = 0;
     bool ok = true;
     Item it;
+    // one half (K: kv = 0, V: kv = 1) of stage src into dst; tok0 = the
+    // stage's first key, t_end = the item's end
+    auto widen = [&](const uint8_t* src, uint8_t* dst, int kv, int tok0, int t_end) {
+      constexpr int kItems = kWTiles * 128;  // (tile, 8-row block, chunk c, row j)
+      constexpr int kCT = 32 * (C::kConverters > 0 ? C::kConverters : 1);  // (bf16: unused)
+#pragma unroll
+      for (int k0 = 0; k0 < (kItems + kCT - 1) / kCT; k0 += 4) {
+        uint4 raw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int idx = ct + (k0 + u) * kCT;
+          if (idx < kItems) {
+            const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
+            const int ti = (idx >> 7) & (kWTiles - 1);
+            raw[u] = *reinterpret_cast<const uint4*>(src + kv * kWTiles * kWF8Tile + ti * kWF8Tile +
+                                                     tin * 128 + ((c ^ j) << 4));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int idx = ct + (k0 + u) * kCT;
+          if (idx < kItems) {
+            const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
+            const int ti = (idx >> 7) & (kWTiles - 1);
+            uint8_t* row = dst + (c >> 2) * kWHalf + (ti * kTileTokens + tin) * 128;
+            const int c0 = (2 * c) & 7;
+            uint4 lo = make_uint4(e4m3x2_to_f16x2(raw[u].x), e4m3x2_to_f16x2(raw[u].x >> 16),
+                                  e4m3x2_to_f16x2(raw[u].y), e4m3x2_to_f16x2(raw[u].y >> 16));
+            uint4 hi = make_uint4(e4m3x2_to_f16x2(raw[u].z), e4m3x2_to_f16x2(raw[u].z >> 16),
+                                  e4m3x2_to_f16x2(raw[u].w), e4m3x2_to_f16x2(raw[u].w >> 16));
+            if (kv == 1 && tok0 + ti * kTileTokens + tin >= t_end) {
+              lo = make_uint4(0u, 0u, 0u, 0u);
+              hi = lo;
+            }
+            *reinterpret_cast<uint4*>(row + ((c0 ^ j) << 4)) = lo;
+            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ j) << 4)) = hi;
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the tensor core reads the widened half
+      __syncwarp();
+    };
     for (int k = 0; ok && schedule_item(sched, a, k, &it); ++k) {
       for (int i = 0; i < it.n_iters; ++i, ++gs) {
         const int s = gs % C::kStages;
-        const int o = gs % C::kOpStages;
-        ok = __all_sync(kFull, mbar_wait(&full_bar[s], (gs / C::kStages) & 1)) != 0;
-        if (ok && gs >= C::kOpStages)
-          ok = __all_sync(kFull, mbar_wait(&conv_empty[o], ((gs / C::kOpStages) - 1) & 1)) != 0;
-        if (!ok) break;
+        const int ok_slot = gs % C::kOpK;
+        const int ov_slot = gs % C::kOpV;
+        const int tok0 = it.t_begin + i * kWTok;
         const uint8_t* src = smem + C::kOffLoad + s * C::kLoadBytes;
-        uint8_t* dst = smem + C::kOffOp + o * kWStageBytes;
-        // item idx: (K or V, tile, 8-row block, chunk c, row j); four loads in
-        // flight before the conversions
-        constexpr int kItems = 2 * kWTiles * 128;
-        constexpr int kCT = 32 * (C::kConverters > 0 ? C::kConverters : 1);  // (bf16: unused)
-#pragma unroll
-        for (int k0 = 0; k0 < (kItems + kCT - 1) / kCT; k0 += 4) {
-          uint4 raw[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int idx = ct + (k0 + u) * kCT;
-            if (idx < kItems) {
-              const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
-              const int ti = (idx >> 7) & (kWTiles - 1), kv = idx >> 9;
-              raw[u] = *reinterpret_cast<const uint4*>(src + kv * kWTiles * kWF8Tile + ti * kWF8Tile +
-                                                       tin * 128 + ((c ^ j) << 4));
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int idx = ct + (k0 + u) * kCT;
-            if (idx < kItems) {
-              const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
-              const int ti = (idx >> 7) & (kWTiles - 1), kv = idx >> 9;
-              uint8_t* row =
-                  dst + kv * 2 * kWHalf + (c >> 2) * kWHalf + (ti * kTileTokens + tin) * 128;
-              const int c0 = (2 * c) & 7;
-              *reinterpret_cast<uint4*>(row + ((c0 ^ j) << 4)) =
-                  make_uint4(e4m3x2_to_f16x2(raw[u].x), e4m3x2_to_f16x2(raw[u].x >> 16),
-                             e4m3x2_to_f16x2(raw[u].y), e4m3x2_to_f16x2(raw[u].y >> 16));
-              *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ j) << 4)) =
-                  make_uint4(e4m3x2_to_f16x2(raw[u].z), e4m3x2_to_f16x2(raw[u].z >> 16),
-                             e4m3x2_to_f16x2(raw[u].w), e4m3x2_to_f16x2(raw[u].w >> 16));
-            }
-          }
-        }
-        fence_proxy_async_smem();  // the tensor core reads the widened stage
-        __syncwarp();
+        ok = __all_sync(kFull, mbar_wait(&full_bar[s], (gs / C::kStages) & 1)) != 0;
+        if (ok && gs >= C::kOpK)
+          ok = __all_sync(kFull, mbar_wait(&convk_empty[ok_slot], ((gs / C::kOpK) - 1) & 1)) != 0;
+        if (!ok) break;
+        widen(src, smem + C::kOffOpK + ok_slot * C::kKSlotBytes, 0, tok0, it.t_end);
+        if (lane == 0) mbar_arrive(&convk_full[ok_slot]);
+        if (gs >= C::kOpV)
+          ok = __all_sync(kFull, mbar_wait(&convv_empty[ov_slot], ((gs / C::kOpV) - 1) & 1)) != 0;
+        if (!ok) break;
+        widen(src, smem + C::kOffOpV + ov_slot * C::kVSlotBytes, 1, tok0, it.t_end);
         if (lane == 0) {
-          mbar_arrive(&conv_full[o]);
+          mbar_arrive(&convv_full[ov_slot]);
           mbar_arrive(&empty_bar[s]);
         }
       }
@@ -594,34 +629,35 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     // B-operand descriptors of stage 0: other stages and K-steps differ only
     // in the start-address field (16-byte units, no carry below 256 KB), so
     // each MMA adds a constant to one of these. A (Q, P) is read from TMEM.
-    const uint64_t k_desc0 = umma_smem_desc(smem_base + C::kOffOp, 16, 1024);
+    const uint64_t k_desc0 = umma_smem_desc(smem_base + C::kOffOpK, 16, 1024);
     // B = V [64 keys][2 x 64 d], MN-major: d-halves 8 KB apart (LBO), 8-key
     // groups 1 KB apart (SBO), 16 keys = 2 KB per K-step
-    const uint64_t v_desc0 = umma_smem_desc(smem_base + C::kOffOp + 2 * kWHalf, kWHalf, 1024);
+    const uint64_t v_desc0 = umma_smem_desc(smem_base + C::kOffOpV, kWHalf, 1024);
     // O += P_jj . V_jj (ring stage gsj), then release the stage and the P buffer
     auto issue_pv = [&](int jj, int gsj) {
       tc_fence_after_sync();
       const uint32_t pa = tmem + kWColP + (jj & 1) * (kWTok / 2);
-      const uint64_t vd = v_desc0 + static_cast<uint64_t>((gsj % C::kOpStages) * (kWStageBytes >> 4));
+      const uint64_t vd = v_desc0 + static_cast<uint64_t>((gsj % C::kOpV) * (C::kVSlotBytes >> 4));
       const uint32_t d = tmem + kWColO + (jj & 1) * kHeadDim;
 #pragma unroll
       for (int kk = 0; kk < kWTok / 16; ++kk)  // 16 keys = 8 P columns per K-step
         umma_bf16_ts_warp(d, pa + kk * 8, vd + kk * (2048 >> 4), kIdescPV,
                           (jj > 1 || kk > 0) ? 1u : 0u);
       umma_commit_warp(&pv_done[jj & 1]);
-      umma_commit_warp(F8 ? &conv_empty[gsj % C::kOpStages] : &empty_bar[gsj % C::kStages]);
+      umma_commit_warp(F8 ? &convv_empty[gsj % C::kOpV] : &empty_bar[gsj % C::kStages]);
     };
     // S_j = Q . K_j^T: 16 d per K-step (8 Q columns; K: d-half kk / 4, 32
     // bytes into its 128-byte swizzled rows)
     auto issue_qk = [&](int j, int gsj) {
       tc_fence_after_sync();
-      const uint64_t kd = k_desc0 + static_cast<uint64_t>((gsj % C::kOpStages) * (kWStageBytes >> 4));
+      const uint64_t kd = k_desc0 + static_cast<uint64_t>((gsj % C::kOpK) * (C::kKSlotBytes >> 4));
       const uint32_t d = tmem + (j & 1) * kWTok;
 #pragma unroll
       for (int kk = 0; kk < kHeadDim / 16; ++kk)
         umma_bf16_ts_warp(d, tmem + kWColQ + kk * 8, kd + (((kk >> 2) * kWHalf + (kk & 3) * 32) >> 4),
                           kIdescQK, kk > 0 ? 1u : 0u);
       umma_commit_warp(&s_full[j & 1]);
+      if constexpr (F8) umma_commit_warp(&convk_empty[gsj % C::kOpK]);  // its K slot is free
     };
     bool ok = true;
     int gs = 0;         // ring stages consumed so far (all items)
@@ -647,7 +683,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
           const int j = next_qk;
           const int gsj = gs + j;
           const int u = ((j & 1) ? u1 : u0) + (j >> 1);  // the group's use of its buffers
-          const bool landed = F8 ? mbar_test(&conv_full[gsj % C::kOpStages], (gsj / C::kOpStages) & 1)
+          const bool landed = F8 ? mbar_test(&convk_full[gsj % C::kOpK], (gsj / C::kOpK) & 1)
                                  : mbar_test(&full_bar[gsj % C::kStages], (gsj / C::kStages) & 1);
           const bool s_ready = u == 0 || mbar_test(&s_free[j & 1], (u - 1) & 1);
           if (__any_sync(kFull, landed) && __any_sync(kFull, s_ready)) {
@@ -659,7 +695,9 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         if (next_pv < next_qk) {
           const int jj = next_pv;
           const int u = ((jj & 1) ? u1 : u0) + (jj >> 1);
-          if (__any_sync(kFull, mbar_test(&p_full[jj & 1], u & 1))) {
+          const int gsv = gs + jj;  // (FP8: its V slot must be widened too)
+          const bool v_ready = !F8 || mbar_test(&convv_full[gsv % C::kOpV], (gsv / C::kOpV) & 1);
+          if (__any_sync(kFull, v_ready) && __any_sync(kFull, mbar_test(&p_full[jj & 1], u & 1))) {
             issue_pv(jj, gs + jj);
             ++next_pv;
             progress = true;
@@ -865,10 +903,11 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         tmem_st32(lane_base + kWColP + grp * (kWTok / 2), w);
       }
       // keys past the chunk end: their V rows may hold anything (NaN * 0 is
-      // NaN), so zero them before the MMA reads the stage
+      // NaN), so zero them before the MMA reads the stage (FP8: the
+      // converters already wrote those rows as zeros)
       const int n_valid = min(kWTok, t_end - tok0);
-      if (n_valid < kWTok) {
-        uint8_t* vst = smem + C::kOffOp + ((gs + j) % C::kOpStages) * kWStageBytes + 2 * kWHalf;
+      if (!F8 && n_valid < kWTok) {
+        uint8_t* vst = smem + C::kOffOpV + ((gs + j) % C::kOpV) * C::kVSlotBytes;
         for (int idx = r; idx < (kWTok - n_valid) * 16; idx += 128) {
           const int row = n_valid + (idx >> 4);
           const int c = idx & 15;  // 8 chunks per half, 2 halves
