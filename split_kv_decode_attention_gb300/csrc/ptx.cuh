@@ -239,6 +239,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return r;
 }
 
+// Four E4M3 bytes to two f16x2 words (bytes 0-1 -> lo, bytes 2-3 -> hi); the
+// word is split into its 16-bit halves in place, with no shift.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four_bytes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_bytes));
+}
+
 // Sum of the two values of a packed bf16x2 (or, with f16 = true, f16x2)
 // pair, in fp32 (exact widening).  The probabilities of the P.V product are
 // rounded to 16 bits; normalising the output by the sum of those rounded

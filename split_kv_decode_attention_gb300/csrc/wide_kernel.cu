@@ -59,11 +59,14 @@ constexpr int kWTiles = kWTok / kTileTokens; // 16-token page tiles per stage
 #ifndef DATTN_WIDE_F8_STAGES
 #define DATTN_WIDE_F8_STAGES 4
 #endif
+#ifndef DATTN_WIDE_F8_QSTAGE
+#define DATTN_WIDE_F8_QSTAGE 0
+#endif
 #ifndef DATTN_WIDE_F8_PRODUCERS
-#define DATTN_WIDE_F8_PRODUCERS 2
+#define DATTN_WIDE_F8_PRODUCERS 3
 #endif
 #ifndef DATTN_WIDE_F8_CONVERTERS
-#define DATTN_WIDE_F8_CONVERTERS 5
+#define DATTN_WIDE_F8_CONVERTERS 4
 #endif
 // FP8: widened K and V live in separate rings (a K slot is free once S =
 // Q.K^T is done, a V slot only after P.V), 16 KB per slot
@@ -90,16 +93,16 @@ static_assert(kWStatFloats * 4 <= kWStatBytes, "statistics buffer");
 // Warp roles and shared-memory layout of the two variants.
 //   bf16 caches: warps 0-7 softmax, 8..12 TMA producers, 13 MMA; the TMA ring
 //     holds the MMA operands directly (5 stages of 32 KB).
-//   FP8 caches: warps 0-7 softmax, 8..9 TMA producers, 10..14 converters,
+//   FP8 caches: warps 0-7 softmax, 8..10 TMA producers, 11..14 converters,
 //     15 MMA; the TMA ring holds FP8 stages (4 x 16 KB: 8 boxes of 2 KB per 64
 //     keys), the converters widen each stage's K into a ring of 2 f16 K slots
 //     and its V into a ring of 4 f16 V slots (16 KB each; the B operands of
 //     kind::f16 must be 16-bit).  A K slot is released as soon as its S =
 //     Q.K^T completes, a V slot only after its P.V, so the two rings hold
 //     each half only as long as it is needed.
-// Shared memory: TMA ring, operand ring (FP8 only), Q staging ([128 rows][16
-// chunks of 16 B], chunk c of row r at c ^ (r & 15)), the groups' merge
-// statistics (two buffers), schedule tables, barriers.
+// Shared memory: TMA ring, K and V operand rings (FP8 only), Q staging (bf16
+// only: [128 rows][16 chunks of 16 B], chunk c of row r at c ^ (r & 15)), the
+// groups' merge statistics (two buffers), schedule tables, barriers.
 // TMA copies issued by one warp are serialised (~130-240 cycles per box), and
 // the time to issue a stage counts against its ring slot, so all producer
 // warps share each stage's boxes.
@@ -124,7 +127,12 @@ struct WCfg {
   static constexpr int kOffOpK = F8 ? kOffLoad + kStages * kLoadBytes : kOffLoad;
   static constexpr int kOffOpV = F8 ? kOffOpK + kOpK * kKSlotBytes : kOffLoad + 2 * kWHalf;
   static constexpr int kOffQ = F8 ? kOffOpV + kOpV * kVSlotBytes : kOffLoad + kStages * kLoadBytes;
-  static constexpr int kOffStat = kOffQ + kWRows * 256;
+  // bf16: each item's query rows are staged in shared memory by the producers
+  // while the previous item runs; FP8: the softmax warps load them from global
+  // memory at the item's start (GB300, fw64: 205 us against 211 us staged --
+  // the FP8 producers then issue only TMA boxes)
+  static constexpr bool kQStaged = !F8 || DATTN_WIDE_F8_QSTAGE;
+  static constexpr int kOffStat = kOffQ + (kQStaged ? kWRows * 256 : 0);
   static constexpr int kOffSched = kOffStat + 2 * kWStatBytes;
   static constexpr int kOffBar = kOffSched + ((kWSchedInts * 4 + 15) & ~15);
   // full[], empty[] of the TMA ring, then (FP8) full[] and empty[] of the K
@@ -443,24 +451,27 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     Item it;
     for (int k = 0; ok && schedule_item(sched, a, k, &it); ++k) {
       // ---- this item's query rows into the staging buffer, one row per lane
-      if (k > 0) {
-        int good = 1;
-        if (lane == 0) good = mbar_wait(q_empty, (k - 1) & 1) ? 1 : 0;
-        if (!__shfl_sync(kFull, good, 0)) {
-          ok = false;
-          break;
+      // (bf16; the FP8 variant's softmax warps load them themselves)
+      if constexpr (C::kQStaged) {
+        if (k > 0) {
+          int good = 1;
+          if (lane == 0) good = mbar_wait(q_empty, (k - 1) & 1) ? 1 : 0;
+          if (!__shfl_sync(kFull, good, 0)) {
+            ok = false;
+            break;
+          }
         }
-      }
-      for (int r = pw_idx * 32 + lane; r < a.rows; r += 32 * C::kProducers) {
-        const int t = r / a.group;
-        const uint16_t* qrow = a.q + static_cast<int64_t>(it.b) * a.q_sb +
-                               static_cast<int64_t>(t) * a.q_st +
-                               static_cast<int64_t>(it.kvh * a.group + (r - t * a.group)) * a.q_sh;
+        for (int r = pw_idx * 32 + lane; r < a.rows; r += 32 * C::kProducers) {
+          const int t = r / a.group;
+          const uint16_t* qrow = a.q + static_cast<int64_t>(it.b) * a.q_sb +
+                                 static_cast<int64_t>(t) * a.q_st +
+                                 static_cast<int64_t>(it.kvh * a.group + (r - t * a.group)) * a.q_sh;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          cp_async16(q_stage + r * 256 + ((c ^ (r & 15)) << 4), qrow + c * 8);
+          for (int c = 0; c < 16; ++c)
+            cp_async16(q_stage + r * 256 + ((c ^ (r & 15)) << 4), qrow + c * 8);
+        }
+        cp_async_arrive(q_full);
       }
-      cp_async_arrive(q_full);
 
       // ---- K/V stages of the item: each producer warp issues its share of
       // every stage's 2 KB boxes (box bx = lane * kProducers + pw_idx) -- bf16:
@@ -537,7 +548,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
   }
 
   // ======================================================= FP8 converters
-  // Widen each landed FP8 stage: its K tiles into the next K slot, then its V
+  // Widen each landed FP8 stage: its K tiles into the next K slot and its V
   // tiles into the next V slot, each an f16 operand ([2 d-halves][64 tokens]
   // [64 d], 128-byte swizzle): 16-byte chunk c of FP8 row t (d = 16c ..
   // 16c+15) becomes 8-d chunks 2c and 2c+1 of d-half c / 4.  Each 8-lane
@@ -550,46 +561,42 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     int gs = 0;
     bool ok = true;
     Item it;
-    // one half (K: kv = 0, V: kv = 1) of stage src into dst; tok0 = the
-    // stage's first key, t_end = the item's end
-    auto widen = [&](const uint8_t* src, uint8_t* dst, int kv, int tok0, int t_end) {
-      constexpr int kItems = kWTiles * 128;  // (tile, 8-row block, chunk c, row j)
-      constexpr int kCT = 32 * (C::kConverters > 0 ? C::kConverters : 1);  // (bf16: unused)
+    // both halves of stage src (K into dst_k, V into dst_v) in one pass;
+    // tok0 = the stage's first key, t_end = the item's end.  Chunk idx =
+    // ct + 128 u of the stage's 1024 (K or V = u / 4, tile = u % 4): each
+    // thread keeps its 8-row block, row j and chunk c for all eight, so the
+    // addresses are a per-thread base plus constants, and all eight loads are
+    // in flight before the first conversion.  (One pass per stage: each
+    // barrier round trip and fence costs about as much as widening a half.)
+    static_assert(!F8 || C::kConverters == 4, "the widening map assumes 128 converter threads");
+    const int cj = ct & 7, cc = (ct >> 3) & 7, ctin = ((ct >> 6) & 1) * 8 + cj;
+    const int c0 = (2 * cc) & 7;
+    const int src_off = ctin * 128 + ((cc ^ cj) << 4);
+    const int dst_off = (cc >> 2) * kWHalf + ctin * 128;
+    const int st_lo = (c0 ^ cj) << 4, st_hi = ((c0 + 1) ^ cj) << 4;
+    auto widen = [&](const uint8_t* src, uint8_t* dst_k, uint8_t* dst_v, int tok0, int t_end) {
+      uint4 raw[8];
 #pragma unroll
-      for (int k0 = 0; k0 < (kItems + kCT - 1) / kCT; k0 += 4) {
-        uint4 raw[4];
+      for (int u = 0; u < 8; ++u)
+        raw[u] = *reinterpret_cast<const uint4*>(src + (u >> 2) * kWTiles * kWF8Tile +
+                                                 (u & 3) * kWF8Tile + src_off);
+      const int v_rows = t_end - tok0;  // V rows at or past this are zeroed
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int idx = ct + (k0 + u) * kCT;
-          if (idx < kItems) {
-            const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
-            const int ti = (idx >> 7) & (kWTiles - 1);
-            raw[u] = *reinterpret_cast<const uint4*>(src + kv * kWTiles * kWF8Tile + ti * kWF8Tile +
-                                                     tin * 128 + ((c ^ j) << 4));
-          }
+      for (int u = 0; u < 8; ++u) {
+        uint8_t* row = (u >= 4 ? dst_v : dst_k) + dst_off + (u & 3) * kTileTokens * 128;
+        uint4 lo, hi;
+        e4m3x4_to_f16x4(raw[u].x, lo.x, lo.y);
+        e4m3x4_to_f16x4(raw[u].y, lo.z, lo.w);
+        e4m3x4_to_f16x4(raw[u].z, hi.x, hi.y);
+        e4m3x4_to_f16x4(raw[u].w, hi.z, hi.w);
+        if (u >= 4 && (u & 3) * kTileTokens + ctin >= v_rows) {
+          lo = make_uint4(0u, 0u, 0u, 0u);
+          hi = lo;
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int idx = ct + (k0 + u) * kCT;
-          if (idx < kItems) {
-            const int j = idx & 7, c = (idx >> 3) & 7, tin = ((idx >> 6) & 1) * 8 + j;
-            const int ti = (idx >> 7) & (kWTiles - 1);
-            uint8_t* row = dst + (c >> 2) * kWHalf + (ti * kTileTokens + tin) * 128;
-            const int c0 = (2 * c) & 7;
-            uint4 lo = make_uint4(e4m3x2_to_f16x2(raw[u].x), e4m3x2_to_f16x2(raw[u].x >> 16),
-                                  e4m3x2_to_f16x2(raw[u].y), e4m3x2_to_f16x2(raw[u].y >> 16));
-            uint4 hi = make_uint4(e4m3x2_to_f16x2(raw[u].z), e4m3x2_to_f16x2(raw[u].z >> 16),
-                                  e4m3x2_to_f16x2(raw[u].w), e4m3x2_to_f16x2(raw[u].w >> 16));
-            if (kv == 1 && tok0 + ti * kTileTokens + tin >= t_end) {
-              lo = make_uint4(0u, 0u, 0u, 0u);
-              hi = lo;
-            }
-            *reinterpret_cast<uint4*>(row + ((c0 ^ j) << 4)) = lo;
-            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ j) << 4)) = hi;
-          }
-        }
+        *reinterpret_cast<uint4*>(row + st_lo) = lo;
+        *reinterpret_cast<uint4*>(row + st_hi) = hi;
       }
-      fence_proxy_async_smem();  // the tensor core reads the widened half
+      fence_proxy_async_smem();  // the tensor core reads the widened halves
       __syncwarp();
     };
     for (int k = 0; ok && schedule_item(sched, a, k, &it); ++k) {
@@ -597,19 +604,16 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         const int s = gs % C::kStages;
         const int ok_slot = gs % C::kOpK;
         const int ov_slot = gs % C::kOpV;
-        const int tok0 = it.t_begin + i * kWTok;
-        const uint8_t* src = smem + C::kOffLoad + s * C::kLoadBytes;
         ok = __all_sync(kFull, mbar_wait(&full_bar[s], (gs / C::kStages) & 1)) != 0;
         if (ok && gs >= C::kOpK)
           ok = __all_sync(kFull, mbar_wait(&convk_empty[ok_slot], ((gs / C::kOpK) - 1) & 1)) != 0;
-        if (!ok) break;
-        widen(src, smem + C::kOffOpK + ok_slot * C::kKSlotBytes, 0, tok0, it.t_end);
-        if (lane == 0) mbar_arrive(&convk_full[ok_slot]);
-        if (gs >= C::kOpV)
+        if (ok && gs >= C::kOpV)
           ok = __all_sync(kFull, mbar_wait(&convv_empty[ov_slot], ((gs / C::kOpV) - 1) & 1)) != 0;
         if (!ok) break;
-        widen(src, smem + C::kOffOpV + ov_slot * C::kVSlotBytes, 1, tok0, it.t_end);
+        widen(smem + C::kOffLoad + s * C::kLoadBytes, smem + C::kOffOpK + ok_slot * C::kKSlotBytes,
+              smem + C::kOffOpV + ov_slot * C::kVSlotBytes, it.t_begin + i * kWTok, it.t_end);
         if (lane == 0) {
+          mbar_arrive(&convk_full[ok_slot]);
           mbar_arrive(&convv_full[ov_slot]);
           mbar_arrive(&empty_bar[s]);
         }
@@ -751,10 +755,42 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       const int t = r / a.group;
       lim = a.causal ? min(t_end, it.L - a.q_len + 1 + t) : t_end;
     }
-    // ---- this item's query row (zeros for padding rows) from the staging
-    // buffer into TMEM lane r: the A operand of S = Q.K^T, d pairs packed in
-    // 64 columns (group 0: one row per thread)
-    if (grp == 0) {
+    // ---- this item's query row (zeros for padding rows) into TMEM lane r:
+    // the A operand of S = Q.K^T, d pairs packed in 64 columns (group 0: one
+    // row per thread).  FP8: straight from global memory, all 16 chunks of the
+    // row in flight at once, widened to f16 (the products run in f16).
+    if (!C::kQStaged && grp == 0) {
+      if (ok) {
+        uint4 v[16];
+        if (r < a.rows) {
+          const int t = r / a.group;
+          const uint4* qrow = reinterpret_cast<const uint4*>(
+              a.q + static_cast<int64_t>(it.b) * a.q_sb + static_cast<int64_t>(t) * a.q_st +
+              static_cast<int64_t>(it.kvh * a.group + (r - t * a.group)) * a.q_sh);
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) v[ch] = __ldg(qrow + ch);
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) v[ch] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int qc = 0; qc < 4; ++qc) {  // 32 d = 16 columns per step
+          uint32_t w[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 x = v[qc * 4 + c];
+            w[4 * c] = bf16x2_to_f16x2(x.x);
+            w[4 * c + 1] = bf16x2_to_f16x2(x.y);
+            w[4 * c + 2] = bf16x2_to_f16x2(x.z);
+            w[4 * c + 3] = bf16x2_to_f16x2(x.w);
+          }
+          tmem_st16(lane_base + kWColQ + qc * 16, w);
+        }
+        tmem_wait_st();
+      }
+    }
+    // (or from the staging buffer the producers filled)
+    if (C::kQStaged && grp == 0) {
       if (ok) ok = __all_sync(kFull, mbar_wait(q_full, k & 1)) != 0;
       if (ok) {
 #pragma unroll 1
