@@ -476,9 +476,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             // r[2h]: key g4, d 4t4..4t4+3 of the step; r[2h+1]: key g4 + 8
-            const uint32_t af[4] = {e4m3x2_to_f16x2(r[2 * h]), e4m3x2_to_f16x2(r[2 * h + 1]),
-                                    e4m3x2_to_f16x2(r[2 * h] >> 16),
-                                    e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+            uint32_t af[4];  // (each word split into its 16-bit halves, no shift)
+            e4m3x4_to_f16x4(r[2 * h], af[0], af[2]);
+            e4m3x4_to_f16x4(r[2 * h + 1], af[1], af[3]);
             uint32_t qb[NT][2];
             q_frag(2 * kp + h, qb);
 #pragma unroll
@@ -582,11 +582,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, STAGES, TPS, F8>::kThreads)
           ldsm_x4_trans(vt + key * 128 + ((chunk ^ (key & 7)) << 4), r);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t af[4] = {
-                e4m3x2_to_f16x2(__byte_perm(r[2 * h], 0, 0x20)),      // d 2g4,     keys 2t4, +1
-                e4m3x2_to_f16x2(__byte_perm(r[2 * h], 0, 0x31)),      // d 2g4 + 1
-                e4m3x2_to_f16x2(__byte_perm(r[2 * h + 1], 0, 0x20)),  // d 2g4,     keys 8 + 2t4, +1
-                e4m3x2_to_f16x2(__byte_perm(r[2 * h + 1], 0, 0x31))}; // d 2g4 + 1
+            // one byte permute per word: (key 2t4, key 2t4 + 1) of d 2g4 in the
+            // low half, of d 2g4 + 1 in the high half; then both halves widen
+            uint32_t af[4];  // d 2g4 / 2g4 + 1 of keys 2t4, +1, then of keys 8 + 2t4, +1
+            e4m3x4_to_f16x4(__byte_perm(r[2 * h], 0, 0x3120), af[0], af[1]);
+            e4m3x4_to_f16x4(__byte_perm(r[2 * h + 1], 0, 0x3120), af[2], af[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_f16_16816(acc[2 * mp + h][nt], af, pb[nt][0], pb[nt][1]);
