@@ -50,6 +50,11 @@ constexpr float kLn2w = 0.6931471805599453f;
 constexpr int kWRows = 128;                  // MMA M: query rows per CTA (padded)
 constexpr int kWTok = 64;                    // keys per stage (MMA N of S)
 constexpr int kWTiles = kWTok / kTileTokens; // 16-token page tiles per stage
+// Pipeline shapes (build-time overridable for sweeps; the defaults are the
+// GB300 sweep winners): TMA ring stages and producer warps for bf16 caches;
+// for FP8 caches also the converter warps, whether the producers stage each
+// item's Q rows in shared memory (else the softmax warps load them), and the
+// K and V operand slots.
 #ifndef DATTN_WIDE_STAGES
 #define DATTN_WIDE_STAGES 5
 #endif
