@@ -402,3 +402,35 @@ def test_withheld_copy_times_out_in_the_tcgen05_kernel_and_context_stays_usable(
     ref_o, ref_l = oracle.decode_attention_inputs(inp)
     assert_out_close(bf16_tensor_to_f64(out), ref_o)
     assert_lse_close(lse.cpu().numpy(), ref_l)
+
+
+def test_withheld_copy_times_out_in_the_fp8_tcgen05_kernel_and_context_stays_usable(binding):
+    """The same on the tcgen05 kernel's FP8 variant, whose converter warps
+    wait on the TMA stage and on free K and V operand slots: CTA 0's first
+    stage never lands, so the converters' bounded waits run out, the MMA
+    warp's idle limit runs out waiting for widened K, and the call reports
+    DA_STATUS_TIMEOUT; the next call on the same context is exact."""
+    import time
+    shp = W.small_shape("withhold_wide_fp8", batch=2, q_len=8, num_q_heads=16, num_kv_heads=2,
+                        lo=500, hi=900, causal=True, seed=72, kv_fp8=True)
+    inp = W.make_host_inputs(shp)
+    q, k, v, bt, lens = to_device(inp)
+    kw = dict(max_seq_len=inp.max_seq_len, causal=True, k_scale=inp.k_scale,
+              v_scale=inp.v_scale)
+    p = binding.params_from_tensors(q, k, bt, two_pass=True, **kw)
+    p.flags |= binding.DA_FLAG_TEST_WITHHOLD_COPY
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    binding.decode_attn(q, k, v, bt, lens, num_splits=2, status=status, params=p,
+                        max_seq_len=inp.max_seq_len, causal=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) & binding.DA_STATUS_TIMEOUT
+    assert time.time() - t0 < 60
+    status.zero_()
+    out, lse = binding.decode_attn(q, k, v, bt, lens, num_splits=2, status=status,
+                                   two_pass=True, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_o, ref_l = oracle.decode_attention_inputs(inp)
+    assert_out_close(bf16_tensor_to_f64(out), ref_o)
+    assert_lse_close(lse.cpu().numpy(), ref_l)
