@@ -43,12 +43,22 @@ struct PlanShape {
   int max_seq_len;   // upper bound of every length (>= 0)
 };
 
-__host__ __device__ inline int64_t plan_ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// a / b for a >= 0, b > 0, in 32 bits when both fit: on the GPU a 64-bit
+// division is a long dependent sequence, and the device planner's path is a
+// chain of them
+__host__ __device__ inline int64_t plan_div(int64_t a, int64_t b) {
+  if (((a | b) >> 32) == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
+__host__ __device__ inline int64_t plan_ceil_div(int64_t a, int64_t b) { return plan_div(a + b - 1, b); }
 
 // a * b, saturated at 2^62 (both >= 0)
 __host__ __device__ inline int64_t plan_sat_mul(int64_t a, int64_t b) {
   const int64_t lim = int64_t{1} << 62;
   if (a == 0 || b == 0) return 0;
+  if (((a | b) >> 31) == 0) return a * b;  // (both below 2^31)
   return a > lim / b ? lim : a * b;
 }
 
@@ -68,6 +78,23 @@ __host__ __device__ inline bool plan_chunk_for_splits(int max_seq_len, int64_t s
   return true;
 }
 
+// The largest c in (lo, hi] with chunks_of(c) >= need, or lo when there is
+// none (lo <= hi; lo itself is never tested).  chunks_of is non-increasing in
+// c, so the lengths that pass are those up to one boundary and every search
+// for it gives the same c.  This one tests hi first (the usual answer), then
+// bisects.
+template <class ChunksOf>
+__host__ __device__ int64_t plan_search_bisect(int64_t lo, int64_t hi, int64_t need,
+                                               ChunksOf&& chunks_of) {
+  if (hi <= lo || chunks_of(hi) >= need) return hi;
+  while (hi - lo > 1) {  // (chunks_of(hi) < need from here on)
+    const int64_t mid = (lo + hi) / 2;
+    if (chunks_of(mid) >= need) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
 // Chunks per (request, kv head) for the batch (before plan_chunk_for_splits).
 //   uniform      all lengths equal, or none known (then max_seq_len is taken)
 //   work_tokens  sum of the clamped lengths (ragged batches only)
@@ -80,16 +107,18 @@ __host__ __device__ inline bool plan_chunk_for_splits(int max_seq_len, int64_t s
 // rows) tokens each (kWideTokensPerRow above 16 rows); a small batch keeps at
 // least one chunk per slot: while that floor leaves fewer chunks than slots,
 // the chunk shrinks to the largest length that fills them (not below 256).
-template <class ChunksOf>
+// search(lo, hi, need) finds that length as plan_search_bisect defines it
+// (the device planner tests several lengths at once; the answer is the same).
+template <class ChunksOf, class Search>
 __host__ __device__ int64_t plan_splits(const PlanShape& s, bool uniform, int64_t work_tokens,
-                                        ChunksOf&& chunks_of) {
+                                        ChunksOf&& chunks_of, Search&& search) {
   const int64_t msl = s.max_seq_len;
   const int64_t max_tiles = plan_ceil_div(msl > 1 ? msl : 1, kPlanTile);
   const int64_t pairs = static_cast<int64_t>(s.batch > 1 ? s.batch : 1) * s.num_kv_heads;
   int64_t splits = 1;
   if (uniform) {
     if (pairs < s.slots) {
-      const int64_t f = s.slots / pairs;
+      const int64_t f = plan_div(s.slots, pairs);
       splits = f < kMaxClusterSplits ? f : kMaxClusterSplits;
     }
   } else {
@@ -98,22 +127,22 @@ __host__ __device__ int64_t plan_splits(const PlanShape& s, bool uniform, int64_
     const int64_t per_row = s.rows > kPlanMaxNarrowRows ? kWideTokensPerRow : kTokensPerRow;
     const int64_t floor_rows = per_row * s.rows;
     const int64_t min_chunk = floor_rows > kMinChunkTokens ? floor_rows : kMinChunkTokens;
-    int64_t target = per_cta > min_chunk ? per_cta : min_chunk;
-    if (target > kMinChunkTokens && chunks_of(target) < s.slots) {
-      int64_t lo = kMinChunkTokens, hi = target;  // chunks_of(hi) < slots
-      while (hi - lo > 1) {
-        const int64_t mid = (lo + hi) / 2;
-        if (chunks_of(mid) >= s.slots) lo = mid;
-        else hi = mid;
-      }
-      target = lo;
-    }
+    const int64_t target = search(int64_t{kMinChunkTokens},
+                                  per_cta > min_chunk ? per_cta : min_chunk, s.slots);
     splits = plan_ceil_div(msl > 1 ? msl : 1, target);
   }
   const int64_t by_min = msl / kMinChunkTokens > 1 ? msl / kMinChunkTokens : 1;
   if (splits > by_min) splits = by_min;
   if (splits > max_tiles) splits = max_tiles;
   return splits > 1 ? splits : 1;
+}
+
+template <class ChunksOf>
+__host__ __device__ int64_t plan_splits(const PlanShape& s, bool uniform, int64_t work_tokens,
+                                        ChunksOf&& chunks_of) {
+  return plan_splits(s, uniform, work_tokens, chunks_of, [&](int64_t lo, int64_t hi, int64_t need) {
+    return plan_search_bisect(lo, hi, need, chunks_of);
+  });
 }
 
 }  // namespace dattn

@@ -93,6 +93,11 @@ def test_device_plan_equals_host_plan_on_benchmark_lengths(binding, name):
     ([1, 300, 0, 17, 5000], 4, 16, 4),
     (list(range(1, 3000, 7)), 1, 4, 1),         # 429 requests
     (list(np.random.default_rng(3).integers(1, 4097, 5000)), 1, 8, 8),  # beyond the smem cache
+    # 24000 (request, kv head) pairs: every planner CTA writes several blocks
+    (list(np.random.default_rng(4).integers(1, 4097, 3000)), 1, 8, 8),
+    # 120 requests on one kv head (fewer pairs than tcgen05 CTAs): the split
+    # search runs with 16 threads testing each candidate
+    (list(np.random.default_rng(5).integers(1, 12000, 120)), 1, 128, 1),
 ])
 def test_device_plan_equals_host_plan_on_shapes(binding, lens, q_len, hq, hkv):
     lens = np.asarray(lens, np.int32)
