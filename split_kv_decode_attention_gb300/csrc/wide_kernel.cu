@@ -32,6 +32,15 @@
 //     the last rescale (P stays <= 256, exact in the deferred normalisation,
 //     §2.1); at the end of an item the two groups merge and write the item's
 //     output, then load the next item's Q into TMEM.
+//     Up to 64 query rows the kernel splits the keys instead of padding the
+//     rows: TMEM lane l holds row 16 (l / 32) + (l % 16) and takes keys
+//     [0, 32) of every tile when l % 32 < 16, else [32, 64), each lane with
+//     its own running max / sum and O row (its P row is zero over the other
+//     half, so P.V sums only its keys; TMEM loads and stores take one column
+//     address per warp, so every lane still moves the whole score and P row).  All 128 lanes then do useful work --
+//     padded rows would leave half the softmax warps computing masked scores
+//     -- and the two halves of a row sit in one warp, 16 lanes apart, where
+//     the end of the item merges them by shuffles.
 // Outputs are the final bf16 rows (single chunk) or fp32 partials + LSE for
 // the combine kernel, exactly like split_kernel.cu.  Every wait is bounded;
 // TMEM is always released before the CTA exits.
@@ -249,7 +258,8 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // P.V accumulates into O[g]; the two groups alternate, so one group's softmax
 // overlaps the other's, and their (m, l, O) merge exactly at the end.  Phases
 // of the ring and of each group's barriers run on across items.
-template <bool F8>
+// KS: key split for items of at most 64 query rows (see the file comment).
+template <bool F8, bool KS>
 __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     wide_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                 const SplitArgs a) {
@@ -745,10 +755,14 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
 
   // ================================================ softmax groups (warps 0-7)
   const int grp = warp >> 2;       // softmax group: tiles j with j & 1 == grp
-  const int r = tid & 127;         // query row = TMEM lane
+  const int r = tid & 127;         // TMEM lane
+  // query row of the lane and (key split) the half of each tile it takes
+  const int row = KS ? ((r >> 5) << 4) | (r & 15) : r;
+  const int kh = KS ? (r >> 4) & 1 : 0;
+  constexpr int kKeys = KS ? kWTok / 2 : kWTok;  // keys of a tile per thread
   const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const uint32_t o_col = kWColO + grp * kHeadDim;
-  const uint8_t* q_stage = smem + C::kOffQ + r * 256;
+  const uint8_t* q_stage = smem + C::kOffQ + row * 256;
   int gs = 0;      // ring stages of all previous items
   int u_base = 0;  // this group's tiles in all previous items
   bool ok = true;
@@ -756,8 +770,8 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
   for (int k = 0; schedule_item(sched, a, k, &it); ++k) {
     const int t_end = it.t_end;
     int lim = 0;  // keys j < lim are visible to this row (0 for padding rows)
-    if (r < a.rows) {
-      const int t = r / a.group;
+    if (row < a.rows) {
+      const int t = row / a.group;
       lim = a.causal ? min(t_end, it.L - a.q_len + 1 + t) : t_end;
     }
     // ---- this item's query row (zeros for padding rows) into TMEM lane r:
@@ -767,11 +781,11 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
     if (!C::kQStaged && grp == 0) {
       if (ok) {
         uint4 v[16];
-        if (r < a.rows) {
-          const int t = r / a.group;
+        if (row < a.rows) {
+          const int t = row / a.group;
           const uint4* qrow = reinterpret_cast<const uint4*>(
               a.q + static_cast<int64_t>(it.b) * a.q_sb + static_cast<int64_t>(t) * a.q_st +
-              static_cast<int64_t>(it.kvh * a.group + (r - t * a.group)) * a.q_sh);
+              static_cast<int64_t>(it.kvh * a.group + (row - t * a.group)) * a.q_sh);
 #pragma unroll
           for (int ch = 0; ch < 16; ++ch) v[ch] = __ldg(qrow + ch);
         } else {
@@ -804,8 +818,8 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int ch = qc * 4 + c;
-            const uint4 v = r < a.rows
-                                ? *reinterpret_cast<const uint4*>(q_stage + ((ch ^ (r & 15)) << 4))
+            const uint4 v = row < a.rows
+                                ? *reinterpret_cast<const uint4*>(q_stage + ((ch ^ (row & 15)) << 4))
                                 : make_uint4(0, 0, 0, 0);
             // FP8 caches: the products run in f16, so Q is widened too
             w[4 * c] = F8 ? bf16x2_to_f16x2(v.x) : v.x;
@@ -839,7 +853,9 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       ok = __all_sync(kFull, mbar_wait(&s_full[grp], u & 1)) != 0;
       if (!ok) break;
       tc_fence_after_sync();
-      float x[kWTok];
+      // (tcgen05.ld and .st take one column address for the whole warp, so
+      // a key-split lane reads the whole score row and keeps its half)
+      float x[kKeys];
       {
         float lo[32], hi[32];
         tmem_ld32(lane_base + grp * kWTok, lo);
@@ -847,8 +863,12 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          x[i] = lo[i];
-          x[32 + i] = hi[i];
+          if constexpr (KS) {
+            x[i] = kh ? hi[i] : lo[i];
+          } else {
+            x[i] = lo[i];
+            x[32 + i] = hi[i];
+          }
         }
       }
       tc_fence_before_sync();
@@ -861,17 +881,18 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       // the max of the raw ones, so the scores stay raw and the scale goes into
       // the exponent's multiply-add below (s_fma; one multiply less per score);
       // any other scale scales them here (s_fma = 1).
-      const int tok0 = it.t_begin + j * kWTok;
+      const int tile0 = it.t_begin + j * kWTok;
+      const int tok0 = tile0 + kh * kKeys;  // this thread's first key
       const bool raw = a.scale_log2 > 0.f;
       const float s_fma = raw ? a.scale_log2 : 1.f;
       float mt = -INFINITY;
       if (raw) {
-        if (tok0 + kWTok <= lim) {
+        if (tok0 + kKeys <= lim) {
 #pragma unroll
-          for (int i = 0; i < kWTok; i += 2) mt = fmax3(mt, x[i], x[i + 1]);
+          for (int i = 0; i < kKeys; i += 2) mt = fmax3(mt, x[i], x[i + 1]);
         } else {
 #pragma unroll
-          for (int i = 0; i < kWTok; i += 2) {
+          for (int i = 0; i < kKeys; i += 2) {
             x[i] = tok0 + i < lim ? x[i] : -INFINITY;
             x[i + 1] = tok0 + i + 1 < lim ? x[i + 1] : -INFINITY;
             mt = fmax3(mt, x[i], x[i + 1]);
@@ -880,7 +901,7 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         mt *= a.scale_log2;
       } else {
 #pragma unroll
-        for (int i = 0; i < kWTok; i += 2) {
+        for (int i = 0; i < kKeys; i += 2) {
           x[i] = tok0 + i < lim ? x[i] * a.scale_log2 : -INFINITY;
           x[i + 1] = tok0 + i + 1 < lim ? x[i + 1] * a.scale_log2 : -INFINITY;
           mt = fmax3(mt, x[i], x[i + 1]);
@@ -892,12 +913,12 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       const float mref = m_used == -INFINITY ? 0.f : m_used;  // all masked so far: p = 0
       // (pairs of scores in the packed two-wide fp32 instructions: half the
       // issue slots for the exponent arguments and the running sums)
-      uint32_t pk[kWTok / 2];
+      uint32_t pk[kKeys / 2];
       float2 ps = make_float2(0.f, 0.f), qs = make_float2(0.f, 0.f);
       const float2 s2 = make_float2(s_fma, s_fma);
       const float2 nm2 = make_float2(-mref, -mref);
 #pragma unroll
-      for (int i = 0; i < kWTok; i += 2) {
+      for (int i = 0; i < kKeys; i += 2) {
         const float2 e = __ffma2_rn(make_float2(x[i], x[i + 1]), s2, nm2);
         const float p0 = ex2(e.x);
         const float p1 = ex2(e.y);
@@ -937,16 +958,24 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
         }
       }
       // P row (64 bf16 packed in 32 columns) into TMEM: the A operand of P.V
+      // (key split: zeros over the other half of the tile)
       {
         float w[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = __uint_as_float(pk[i]);
+        for (int i = 0; i < 32; ++i) {
+          if constexpr (KS) {
+            const uint32_t v = i < 16 ? (kh ? 0u : pk[i]) : (kh ? pk[i - 16] : 0u);
+            w[i] = __uint_as_float(v);
+          } else {
+            w[i] = __uint_as_float(pk[i]);
+          }
+        }
         tmem_st32(lane_base + kWColP + grp * (kWTok / 2), w);
       }
       // keys past the chunk end: their V rows may hold anything (NaN * 0 is
       // NaN), so zero them before the MMA reads the stage (FP8: the
       // converters already wrote those rows as zeros)
-      const int n_valid = min(kWTok, t_end - tok0);
+      const int n_valid = min(kWTok, t_end - tile0);
       if (!F8 && n_valid < kWTok) {
         uint8_t* vst = smem + C::kOffOpV + ((gs + j) % C::kOpV) * C::kVSlotBytes;
         for (int idx = r; idx < (kWTok - n_valid) * 16; idx += 128) {
@@ -996,26 +1025,43 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
                                                                   //  unless a wait ran out)
     const float m0 = stat[r], l0 = stat[128 + r], q0 = stat[256 + r];
     const float m1 = stat[384 + r], l1 = stat[512 + r], q1 = stat[640 + r];
-    const float M = fmaxf(m0, m1);
+    float M = fmaxf(m0, m1);
+    // key split: the other half of this row is lane r ^ 16 of this warp
+    float pm0 = -INFINITY, pl0 = 0.f, pq0 = 0.f, pm1 = -INFINITY, pl1 = 0.f, pq1 = 0.f;
+    if constexpr (KS) {
+      pm0 = __shfl_xor_sync(kFull, m0, 16);
+      pl0 = __shfl_xor_sync(kFull, l0, 16);
+      pq0 = __shfl_xor_sync(kFull, q0, 16);
+      pm1 = __shfl_xor_sync(kFull, m1, 16);
+      pl1 = __shfl_xor_sync(kFull, l1, 16);
+      pq1 = __shfl_xor_sync(kFull, q1, 16);
+      M = fmaxf(M, fmaxf(pm0, pm1));
+    }
     const float Mu = M == -INFINITY ? 0.f : M;
     const float f0 = l0 > 0.f ? ex2(m0 - Mu) : 0.f;
     const float f1 = l1 > 0.f ? ex2(m1 - Mu) : 0.f;
-    const float Lt = l0 * f0 + l1 * f1;  // the LSE's sum
-    const float Qt = q0 * f0 + q1 * f1;  // the weights P.V actually used
+    float Lt = l0 * f0 + l1 * f1;  // the LSE's sum
+    float Qt = q0 * f0 + q1 * f1;  // the weights P.V actually used
+    if constexpr (KS) {
+      const float pf0 = pl0 > 0.f ? ex2(pm0 - Mu) : 0.f;
+      const float pf1 = pl1 > 0.f ? ex2(pm1 - Mu) : 0.f;
+      Lt += pl0 * pf0 + pl1 * pf1;
+      Qt += pq0 * pf0 + pq1 * pf1;
+    }
     const float inv = (Qt > 0.f ? 1.f / Qt : 0.f) * (F8 ? a.v_scale : 1.f);
     const bool have0 = ok && n_iters > 0;  // O[0] / O[1] were written
     const bool have1 = ok && n_iters > 1;
     const bool direct = it.nsplit == 1;
     const int S = a.num_splits;
-    const int t = r < a.rows ? r / a.group : 0;
-    const int h = it.kvh * a.group + (r - t * a.group);
+    const int t = row < a.rows ? row / a.group : 0;
+    const int h = it.kvh * a.group + (row - t * a.group);
     const int64_t prow = (static_cast<int64_t>(it.b) * a.q_len + t) * a.num_q_heads + h;
     // partial slot of this row: by item for a device-planned call (item =
     // pre[b] * Hkv + kvh * n_b + chunk), else by (row, chunk)
     const int64_t pidx =
         direct ? 0
         : listed ? (static_cast<int64_t>(a.pre[it.b]) * a.num_kv_heads +
-                    static_cast<int64_t>(it.kvh) * it.nsplit + it.split) * a.rows + r
+                    static_cast<int64_t>(it.kvh) * it.nsplit + it.split) * a.rows + row
                  : prow * S + it.split;
     // (O is read out here, before this thread's next arrival on item_go lets
     // the next item's P.V overwrite it)
@@ -1029,28 +1075,43 @@ __global__ void __launch_bounds__(WCfg<F8>::kThreads, 1)
       tmem_ld32(lane_base + kWColO + d0, o0);
       tmem_ld32(lane_base + kWColO + kHeadDim + d0, o1);
       tmem_wait_ld();
-      if (r < a.rows) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          o0[i] = ((have0 ? o0[i] * f0 : 0.f) + (have1 ? o1[i] * f1 : 0.f)) * inv;
+      for (int i = 0; i < 32; ++i) o0[i] = (have0 ? o0[i] * f0 : 0.f) + (have1 ? o1[i] * f1 : 0.f);
+      if constexpr (KS) {
+        // this lane writes columns [d0 + 16 kh, d0 + 16 kh + 16) of the row:
+        // its own sum there plus the other half's, which it receives for the
+        // columns it sends (every lane of the warp takes part)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float mine = kh ? o0[16 + i] : o0[i];
+          const float theirs = __shfl_xor_sync(kFull, kh ? o0[i] : o0[16 + i], 16);
+          o0[i] = (mine + theirs) * inv;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o0[i] *= inv;
+      }
+      constexpr int kCols = KS ? 16 : 32;  // columns this thread writes
+      const int dw = d0 + kh * kCols;
+      if (row < a.rows) {
         if (direct) {
           uint16_t* dst = a.out + static_cast<int64_t>(it.b) * a.o_sb +
-                          static_cast<int64_t>(t) * a.o_st + static_cast<int64_t>(h) * a.o_sh + d0;
+                          static_cast<int64_t>(t) * a.o_st + static_cast<int64_t>(h) * a.o_sh + dw;
 #pragma unroll
-          for (int i = 0; i < 32; i += 8)
+          for (int i = 0; i < kCols; i += 8)
             *reinterpret_cast<uint4*>(dst + i) =
                 make_uint4(pack_bf16x2(o0[i], o0[i + 1]), pack_bf16x2(o0[i + 2], o0[i + 3]),
                            pack_bf16x2(o0[i + 4], o0[i + 5]), pack_bf16x2(o0[i + 6], o0[i + 7]));
         } else {
-          float* dst = a.part_o + pidx * kHeadDim + d0;
+          float* dst = a.part_o + pidx * kHeadDim + dw;
           const uint64_t keep = l2_evict_last_policy();
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
+          for (int i = 0; i < kCols; i += 4)
             st_global_hint(dst + i, make_float4(o0[i], o0[i + 1], o0[i + 2], o0[i + 3]), keep);
         }
       }
     }
-    if (grp == 0 && r < a.rows) {
+    if (grp == 0 && kh == 0 && row < a.rows) {
       const float lse = Lt > 0.f ? (Mu + log2f(Lt)) * kLn2w : -INFINITY;
       if (direct)
         a.lse[prow] = lse;
@@ -1078,7 +1139,10 @@ cudaError_t ensure_wide_attrs(int* sms) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_wide_mu);
   if (!g_wide_attr[F8][dev]) {
-    e = cudaFuncSetAttribute(wide_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(wide_kernel<F8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             WCfg<F8>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(wide_kernel<F8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              WCfg<F8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&g_wide_sms[dev], cudaDevAttrMultiProcessorCount, dev);
@@ -1115,7 +1179,9 @@ cudaError_t launch_wide_t(const CUtensorMap& k_map, const CUtensorMap& v_map, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, wide_kernel<F8>, k_map, v_map, pa);
+  // up to 64 query rows: the key-split form
+  return a.rows <= kWRows / 2 ? cudaLaunchKernelEx(&cfg, wide_kernel<F8, true>, k_map, v_map, pa)
+                              : cudaLaunchKernelEx(&cfg, wide_kernel<F8, false>, k_map, v_map, pa);
 }
 
 }  // namespace
@@ -1136,7 +1202,7 @@ int wide_ctas_per_sm() {
     if (cached[dev] > 0) return cached[dev];
   }
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wide_kernel<false>, WCfg<false>::kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, wide_kernel<false, false>, WCfg<false>::kThreads,
                                                     WCfg<false>::kSmemBytes) != cudaSuccess ||
       n < 1)
     return 1;
