@@ -26,8 +26,11 @@ constexpr int kMinChunkTokens = 256;
 constexpr int kRaggedWaves = 8;
 constexpr int kTokensPerRow = 64;
 // The tcgen05 kernel (17..128 rows) pays ~3 us per work item (epilogue,
-// the two softmax groups' merge), so its chunks hold twice that.
-constexpr int kWideTokensPerRow = 128;
+// the two softmax groups' merge) and writes 512 B of partial output per row
+// of a split item, so its chunks hold four times as many tokens per row.
+// (GB300, 64 rows: one chunk per request 198 us against two 205 us; 128
+// rows keep two chunks, where the floor gives way to filling the SMs.)
+constexpr int kWideTokensPerRow = 256;
 // Largest thread-block cluster the split kernel uses (non-portable size).
 constexpr int kMaxClusterSplits = 16;
 // Tokens per TMA box / MMA tile: chunk lengths are multiples of it.

@@ -22,9 +22,9 @@ BENCH_PLANS = {
     "c5_b32_q4_causal_h32kv8_L1024-16384_paged": (16, 1024),
     "f2_b1_mha32_L131072_fp8": (16, 8192),
     "f5_b32_q4_causal_h32kv8_L1024-16384_paged_fp8": (16, 976),
-    "w64_b32_q8_h64kv8_causal_L1024-16384_paged": (2, 8080),
+    "w64_b32_q8_h64kv8_causal_L1024-16384_paged": (1, 16144),
     "w128_b16_q16_h64kv8_causal_L1024-16384_paged": (2, 7392),
-    "fw64_b32_q8_h64kv8_causal_L1024-16384_paged_fp8": (2, 8128),
+    "fw64_b32_q8_h64kv8_causal_L1024-16384_paged_fp8": (1, 16256),
 }
 
 
@@ -105,7 +105,7 @@ def test_ragged_chunks_hold_the_per_row_floor_when_the_gpu_is_full(q_len, hq, hk
     r = rows(hq, hkv, q_len)
     p = params(256, q_len, hq, hkv, int(lens.max()), 16, causal=q_len > 1)
     S, chunk = binding.decode_attn_plan_slots(p, lens, slots_for(r))
-    floor = max(256, (128 if r > 16 else 64) * r)
+    floor = max(256, (256 if r > 16 else 64) * r)
     msl = int(lens.max())
     # chunks of at least `floor` tokens: no more splits than that allows (the
     # final chunk is max_seq_len / splits rounded up to 16 tokens)
