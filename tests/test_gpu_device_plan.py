@@ -98,6 +98,11 @@ def test_device_plan_equals_host_plan_on_benchmark_lengths(binding, name):
     # 120 requests on one kv head (fewer pairs than tcgen05 CTAs): the split
     # search runs with 16 threads testing each candidate
     (list(np.random.default_rng(5).integers(1, 12000, 120)), 1, 128, 1),
+    # 16 rows on one kv head, short requests: the chunks at the per-row floor
+    # do not fill the CTAs, so the search runs -- 256 requests (a warp per
+    # candidate) and 257 (the bisection with block sums)
+    (list(np.random.default_rng(6).integers(4, 2000, 256)), 4, 4, 1),
+    (list(np.random.default_rng(7).integers(4, 2000, 257)), 4, 4, 1),
 ])
 def test_device_plan_equals_host_plan_on_shapes(binding, lens, q_len, hq, hkv):
     lens = np.asarray(lens, np.int32)
