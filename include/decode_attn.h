@@ -185,7 +185,7 @@ int decode_attn_plan(const decode_attn_params *p, const int32_t *host_seq_lens,
  *                  most 16 query rows per kv head, x 1 above 16 rows)
  * Equal lengths (or host_seq_lens NULL): one wave of equal chunks, at most 16
  * per (request, kv head).  Ragged lengths: chunks for about eight waves of
- * the real work, at least max(256, 64 x rows) tokens (128 x rows above 16
+ * the real work, at least max(256, 64 x rows) tokens (256 x rows above 16
  * rows), shrunk (not below 256) while that leaves fewer chunks than resident
  * CTAs.  Returns DA_ERR_BAD_SHAPE unless 1 <= resident_ctas <= 2^31.
  */
@@ -235,7 +235,7 @@ int decode_attn_workspace_bytes(const decode_attn_params *p, int32_t num_splits,
  * Device planning (num_splits <= 0 with two or more requests; for the
  * tcgen05 kernel, above 16 rows per kv head, at most 1024 requests).  The
  * lengths may exist only on the device -- and change between replays of a
- * captured graph -- so the call plans there: a one-CTA planner kernel applies
+ * captured graph -- so the call plans there: a planner kernel applies
  * decode_attn_plan()'s rule to the current seq_lens (the same plan the host
  * planner gives for those lengths), then the split kernel runs one CTA per
  * item slot of a capacity fixed by the shape (B x Hkv + 16 waves of resident

@@ -51,7 +51,8 @@ struct SplitArgs {
   int item_slots;
 };
 
-// Arguments of the device planner kernel (one CTA; plan_kernel.cu).
+// Arguments of the device planner kernel (plan_kernel.cu; up to 32 CTAs, each
+// running the whole plan and writing its share of the item list).
 struct PlanArgs {
   const int32_t* seq_lens;
   int32_t* status;                     // optional
@@ -142,7 +143,7 @@ int wide_ctas_per_sm();
 // Launch the combine kernel (one warp per output row).
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
-// Launch the device planner (one CTA) ahead of a device-planned split launch.
+// Launch the device planner ahead of a device-planned split launch.
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 
 }  // namespace dattn
