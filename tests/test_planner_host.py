@@ -157,3 +157,48 @@ def test_plan_arguments_are_checked():
     bad.head_dim = 64
     with pytest.raises(binding.DecodeAttnError):
         binding.decode_attn_plan_slots(bad, None, NARROW_SLOTS)
+
+
+def brute_force_plan(lens, hkv, rows, msl, slots):
+    """The planner's rule as its documentation states it, with the split
+    search done by brute force: every candidate chunk length tested."""
+    lens = np.asarray(lens, np.int64)
+    L = np.clip(lens, 0, msl)
+    uniform = bool(np.all(lens == lens[0]))
+    pairs = max(len(lens), 1) * hkv
+    max_tiles = -(-max(msl, 1) // 16)
+    if uniform:
+        splits = min(slots // pairs, 16) if pairs < slots else 1
+    else:
+        per_cta = -(-int(L.sum()) * hkv // (8 * slots))
+        min_chunk = max((256 if rows > 16 else 64) * rows, 256)
+        hi = max(per_cta, min_chunk)
+        cs = np.arange(hi, 256, -1, dtype=np.int64)          # (256, hi], longest first
+        counts = np.where(L[:, None] > 0, -(-L[:, None] // cs[None, :]), 1).sum(axis=0) * hkv
+        ok = np.nonzero(counts >= slots)[0]
+        target = int(cs[ok[0]]) if len(ok) else 256
+        splits = -(-max(msl, 1) // target)
+    splits = max(1, min(splits, max(msl // 256, 1), max_tiles))
+    chunk = -(-(-(-max(msl, 1) // splits)) // 16) * 16
+    return max(1, -(-msl // chunk)), chunk              # (chunks at max_seq_len, length)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_split_search_equals_brute_force(seed):
+    """The host planner's split search (test the top, then bisect) gives the
+    length a scan of every candidate gives, over ragged and equal batches,
+    narrow and wide query groups and slot counts that make it search."""
+    rng = np.random.default_rng(300 + seed)
+    B = int(rng.integers(1, 65))
+    hkv = int(rng.choice([1, 2, 8]))
+    q_len, hq = [(1, 4 * hkv), (4, 4 * hkv), (8, 8 * hkv), (16, 8 * hkv)][int(rng.integers(0, 4))]
+    hi = int(rng.choice([300, 3000, 20000, 50000]))
+    lens = rng.integers(0, hi, B).astype(np.int32)
+    if rng.random() < 0.2:
+        lens[:] = lens[0]                                  # equal lengths
+    msl = max(16, int(lens.max()))
+    rows = hq // hkv * q_len
+    slots = int(rng.choice([152, 608, 1000, 5000]))
+    p = params(B, q_len, hq, hkv, msl, 16, causal=False)
+    got = binding.decode_attn_plan_slots(p, lens, slots)
+    assert got == brute_force_plan(lens, hkv, rows, msl, slots), (B, hkv, rows, msl, slots)
